@@ -1,0 +1,178 @@
+/*
+ * moe_gb300.h -- C ABI of libmoe_gb300.so: one routed Mixture-of-Experts FFN
+ * layer with IQ4_NL expert weights and a sigmoid router, for one NVIDIA
+ * GB300 GPU (sm_103a).
+ *
+ * What the layer computes (HelloSun/xing4_0-29b-IQ4_NL_EPQ model card,
+ * sections "模型與路由" and "對純 NumPy：整層"; PocketLLM "Xing4.0-29B-A4B: the
+ * design record", sections 1, 2 and 4; zhuai.tech "FFN: feature processing
+ * inside each layer"), for each token t with input row x[t]:
+ *
+ *   l[e]  = x[t] . Wr[e]  (+ b[t][e])             router logits, fp32
+ *   s[e]  = sigmoid(l[e])
+ *   S     = the k experts with the largest s, in descending order
+ *   w[j]  = scale * s[S_j] / sum_{i in S} s[i]   (scale = 2.0 for Xing4)
+ *   FFN_e(v) = Down_e( silu(Gate_e v) * (Up_e v) ),  silu(g) = g / (1 + e^-g)
+ *   out[t] = sum_j w[j] * FFN_{S_j}(x[t]) + FFN_shared(x[t])
+ *
+ * Each expert matrix is IQ4_NL: rows of 18-byte blocks, each block one fp16
+ * scale d followed by 16 bytes holding 32 4-bit indices i; weight = d *
+ * table[i] with the 16-entry table {-127,-104,-83,-65,-49,-35,-22,-10,1,13,
+ * 25,38,53,69,89,113}.  Within a block, weight j (0..15) is the low nibble
+ * of index byte j and weight j+16 its high nibble.
+ *
+ * Conventions for every entry point:
+ *   - Every data pointer is a DEVICE pointer owned by the caller, unless the
+ *     argument says otherwise.  Arrays are dense and row-major.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     Route and forward calls are asynchronous on it; they never allocate,
+ *     never synchronise and never copy data back to the host, so they can be
+ *     captured in a CUDA graph.
+ *   - Host-checkable errors (NULL pointer, bad size, T > max_tokens,
+ *     misaligned base pointer) return a status and launch nothing.  Errors
+ *     only the device can see (an expert id outside [0, E) handed to
+ *     moe_forward, a device wait that gave up) set a sticky word in the layer
+ *     that moe_layer_check() reports; the offending route contributes zero.
+ *   - A layer is used by one stream at a time; separate layers are
+ *     independent.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_GB300_ABI_VERSION 1
+
+typedef struct moe_layer_s *moe_layer_t; /* opaque, owned by the library */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,       /* NULL pointer, negative size, bad enum   */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the limits below          */
+  MOE_ERR_MISALIGNED = 3,        /* a base pointer breaks its alignment rule*/
+  MOE_ERR_OUT_OF_MEMORY = 4,     /* cudaMalloc failed in create             */
+  MOE_ERR_CUDA = 5,              /* a CUDA call failed; see moe_last_error  */
+  MOE_ERR_TIMEOUT = 6,           /* a bounded device wait gave up           */
+  MOE_ERR_BAD_EXPERT_ID = 7,     /* an id outside [0, E) reached forward    */
+  MOE_ERR_TOO_MANY_TOKENS = 8    /* T > max_tokens given at create          */
+} moe_status;
+
+typedef enum { MOE_DT_BF16 = 0, MOE_DT_FP32 = 1 } moe_dtype;
+
+/* Layer shape.  Limits: hidden and expert_ffn multiples of 32 in [32, 16384];
+ * 1 <= n_experts <= 256; 1 <= top_k <= min(n_experts, 8); n_shared 0 or 1;
+ * 1 <= max_tokens <= 65536; routed_scaling > 0; flags must be 0. */
+typedef struct {
+  int32_t hidden;       /* H                                                */
+  int32_t n_experts;    /* E routed experts                                 */
+  int32_t top_k;        /* k experts per token                              */
+  int32_t expert_ffn;   /* F, intermediate width of every expert            */
+  int32_t n_shared;     /* 1: one always-on shared expert, weight 1         */
+  float routed_scaling; /* scale applied to the renormalised weights        */
+  int32_t max_tokens;   /* largest T any later call may pass                */
+  uint32_t flags;       /* reserved, must be 0                              */
+} moe_shapes;
+
+/* Expert weights in IQ4_NL blocks (18 bytes each, no alignment needed).
+ *   up, gate: [E][F][H/32] blocks     down: [E][H][F/32] blocks
+ *   sh_up, sh_gate: [F][H/32]         sh_down: [H][F/32]  (NULL if no shared)
+ * The library copies and re-lays them out; see moe_layer_create. */
+typedef struct {
+  const void *up;
+  const void *gate;
+  const void *down;
+  const void *sh_up;
+  const void *sh_gate;
+  const void *sh_down;
+} moe_weights;
+
+/* Create a layer.  Copies the weights into library-owned device memory in an
+ * internal layout (same byte count: 8 blocks' scales and nibbles grouped in
+ * 144-byte units, rows padded with zero blocks to a multiple of 256 weights
+ * where H or F is not one) and allocates every workspace later calls need for
+ * up to max_tokens tokens.  Runs on `stream` and synchronises it before
+ * returning, so the caller may free its weight buffers afterwards.
+ * On success *out holds the layer; on failure *out is NULL and nothing is
+ * leaked. */
+moe_status moe_layer_create(const moe_shapes *shapes, const moe_weights *weights,
+                            void *stream, moe_layer_t *out);
+
+/* Free a layer and its device memory (synchronises the device first).
+ * NULL is accepted and ignored. */
+moe_status moe_layer_destroy(moe_layer_t layer);
+
+/* Router (steps: logits, sigmoid, top-k, renormalise, scale).
+ *   x           [T][H], MOE_DT_BF16 or MOE_DT_FP32, 16-byte aligned
+ *   router_w    [E][H] fp32, 16-byte aligned (the layer's ffn_gate_inp)
+ *   logit_bias  NULL, or fp32 with row t at logit_bias + t*bias_row_stride
+ *               (stride 0: one [E] row for every token), 16-byte aligned;
+ *               added to the logit before the sigmoid
+ *   ids         [T][k] int32 out, descending score; equal scores -> lower id
+ *   weights     [T][k] fp32 out, sum to routed_scaling per token
+ * 0 <= T <= max_tokens; T == 0 returns MOE_OK and launches nothing. */
+moe_status moe_route(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
+                     const float *router_w, const float *logit_bias,
+                     int64_t bias_row_stride, int32_t *ids, float *weights,
+                     void *stream);
+
+/* Expert part of the layer for given routes (steps: per-expert histogram,
+ * prefix sum and permutation; gather; dequantising up/gate projection with
+ * SwiGLU; down projection; weighted combine with the shared expert).
+ *   x        [T][H] as in moe_route
+ *   ids      [T][k] int32, each in [0, E); 4-byte aligned
+ *   weights  [T][k] fp32, any values; 4-byte aligned
+ *   out      [T][H], MOE_DT_BF16 or MOE_DT_FP32, 16-byte aligned; the sum is
+ *            formed in fp32 and rounded once (bf16: nearest-even)
+ * The routed sum and the shared expert are accumulated in fp32 in any order
+ * (fp32 additions of up to k+1 terms per element; not bit-reproducible
+ * between runs). */
+moe_status moe_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
+                       const int32_t *ids, const float *weights, void *out,
+                       moe_dtype out_dtype, void *stream);
+
+/* moe_route followed by moe_forward on the same stream, with the same
+ * arguments; ids and weights are written as by moe_route.  For small T the
+ * two run fused in as few launches as the layer allows. */
+moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype x_dtype,
+                                    int32_t T, const float *router_w,
+                                    const float *logit_bias, int64_t bias_row_stride,
+                                    int32_t *ids, float *weights, void *out,
+                                    moe_dtype out_dtype, void *stream);
+
+/* Residual update and RMS normalisation between stacked layers (PocketLLM
+ * design record, section 2: the residual stream is carried in fp32 and the
+ * sublayer gets the narrow type):
+ *   resid[t] += delta[t]   (skipped when delta is NULL)
+ *   u[t] = bf16( resid[t] / sqrt(mean_c(resid[t][c]^2) + eps) )
+ *   resid [T][H] fp32 in/out; delta [T][H] bf16 or fp32; u [T][H] bf16 out.
+ * All three 16-byte aligned; H a multiple of 8; T >= 0. */
+moe_status moe_residual_rmsnorm(float *resid, const void *delta, moe_dtype delta_dtype,
+                                void *u, int32_t T, int32_t H, float eps, void *stream);
+
+/* Synchronise the device and report (then clear) the layer's sticky device
+ * error: MOE_OK, MOE_ERR_BAD_EXPERT_ID or MOE_ERR_TIMEOUT. */
+moe_status moe_layer_check(moe_layer_t layer);
+
+/* Bytes of IQ4_NL weights held for the layer (routed + shared). */
+int64_t moe_layer_weight_bytes(moe_layer_t layer);
+
+/* Number of kernels this library has launched in the process so far (all
+ * layers, all threads).  Diagnostics: lets a caller count launches per call. */
+int64_t moe_launch_count(void);
+
+/* Static name of a status code. */
+const char *moe_status_string(moe_status status);
+
+/* Detail of the last error returned on the calling thread (static storage,
+ * overwritten by the next failing call on that thread). */
+const char *moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,77 @@
+"""Seeded parity cases -- TEST INFRASTRUCTURE ONLY.
+
+Draws a workload's inputs with the product-independent generator
+(``quantized_moe_expert_sigmoid_gb300.synth``) and redraws any token whose
+routing would be ambiguous: a token is kept only when, among its k+1 largest
+sigmoid scores (fp64, from this oracle's router), adjacent scores differ by
+at least ``GAP``.  That keeps the selected set and its order unique, so a
+kernel computing the logits in fp32 must return the same ids bit for bit.
+"""
+from __future__ import annotations
+
+import dataclasses
+import numpy as np
+
+from quantized_moe_expert_sigmoid_gb300 import synth
+from . import route, to_f64, min_topk_gap
+
+GAP = 1e-4
+
+
+@dataclasses.dataclass
+class Case:
+    wl: synth.Workload
+    x: np.ndarray          # bf16 bits (uint16) or fp32, [T, H]
+    x64: np.ndarray        # the same values in fp64
+    wr: np.ndarray         # fp32 [E, H]
+    bias: np.ndarray | None  # fp32 [T, E] or None
+    ew: synth.ExpertWeights
+    ids: np.ndarray        # oracle routes, int32 [T, k]
+    w: np.ndarray          # oracle weights, fp64 [T, k]
+    logits: np.ndarray     # fp64 [T, E]
+    attempts: np.ndarray
+
+
+def draw_routed_inputs(wl: synth.Workload, wr: np.ndarray, seed: int = 0,
+                       layer: int = 0, T: int | None = None,
+                       bias: np.ndarray | None = None, tag: str = "x",
+                       max_rounds: int = 64):
+    """x for T tokens with every token's top-k+1 scores >= GAP apart."""
+    T = wl.T if T is None else T
+    attempts = np.zeros(T, dtype=np.int64)
+    x = synth.activations(seed, tag, T, wl.H, attempts, wl.x_dtype, layer)
+    x64 = to_f64(x, wl.x_dtype)
+    ids, w, logits = route(x64, wr, wl.k, wl.scale, bias)
+    for _ in range(max_rounds):
+        bad = np.nonzero(min_topk_gap(logits, wl.k) < GAP)[0]
+        if bad.size == 0:
+            return x, x64, ids, w, logits, attempts
+        attempts[bad] += 1
+        # regenerate only the ambiguous rows
+        xb = np.stack([_row(seed, tag, wl, layer, int(t), int(attempts[t])) for t in bad])
+        x[bad] = xb
+        x64[bad] = to_f64(xb, wl.x_dtype)
+        bb = None if bias is None else bias[bad]
+        i2, w2, l2 = route(x64[bad], wr, wl.k, wl.scale, bb)
+        ids[bad], w[bad], logits[bad] = i2, w2, l2
+    raise RuntimeError("could not draw tie-free routing inputs")
+
+
+def _row(seed, tag, wl, layer, t, attempt):
+    """Row t of the activation stream at the given attempt."""
+    key = synth.stream_key(seed, tag, layer, t, attempt)
+    v = synth.normal(key, wl.H)
+    return synth.to_bf16_bits(v) if wl.x_dtype == "bf16" else v.astype(np.float32)
+
+
+def make_case(wl: synth.Workload | str, seed: int = 0, layer: int = 0,
+              T: int | None = None, ew: synth.ExpertWeights | None = None) -> Case:
+    if isinstance(wl, str):
+        wl = synth.WORKLOADS[wl]
+    T = wl.T if T is None else T
+    wr = synth.router_weights(seed, layer, wl.E, wl.H, wl.router_sigma)
+    bias = synth.zipf_logit_bias(seed, T, wl.E) if wl.zipf else None
+    if ew is None:
+        ew = synth.expert_weights(seed, layer, wl.E, wl.H, wl.F, wl.n_shared)
+    x, x64, ids, w, logits, att = draw_routed_inputs(wl, wr, seed, layer, T, bias)
+    return Case(wl, x, x64, wr, bias, ew, ids, w, logits, att)

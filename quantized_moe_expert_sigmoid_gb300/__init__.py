@@ -1,0 +1,249 @@
+"""GB300-native routed IQ4_NL Mixture-of-Experts layer with a sigmoid router.
+
+A thin ctypes binding over libmoe_gb300.so (include/moe_gb300.h).  The
+functions below have the C entry points' names and only marshal arguments:
+torch tensors on the GPU become device pointers, the current torch CUDA
+stream becomes the stream argument, and a non-OK status raises MoeError.
+Every step of the layer runs in the library's CUDA kernels; there is no
+other implementation to fall back to, and importing the library fails
+loudly when it has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB as _LIB_PATH
+
+MOE_OK = 0
+MOE_DT_BF16 = 0
+MOE_DT_FP32 = 1
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
+          3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_OUT_OF_MEMORY", 5: "MOE_ERR_CUDA",
+          6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_BAD_EXPERT_ID", 8: "MOE_ERR_TOO_MANY_TOKENS"}
+
+EXPORTS = ["moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
+           "moe_layer_forward_routed", "moe_residual_rmsnorm", "moe_layer_check",
+           "moe_layer_weight_bytes", "moe_launch_count", "moe_status_string", "moe_last_error"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        self.name = STATUS.get(status, f"status {status}")
+        super().__init__(f"{self.name}: {detail}")
+
+
+class _Shapes(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("expert_ffn", ctypes.c_int32),
+                ("n_shared", ctypes.c_int32), ("routed_scaling", ctypes.c_float),
+                ("max_tokens", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+class _Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("up", "gate", "down", "sh_up", "sh_gate", "sh_down")]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load libmoe_gb300.so (built by build.build()); raises if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"libmoe_gb300.so is not built ({path}); run "
+                           "quantized_moe_expert_sigmoid_gb300.build.build() first")
+    lib = ctypes.CDLL(path)
+    P, I32, I64, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    lib.moe_layer_create.argtypes = [ctypes.POINTER(_Shapes), ctypes.POINTER(_Weights), P,
+                                     ctypes.POINTER(P)]
+    lib.moe_layer_destroy.argtypes = [P]
+    lib.moe_route.argtypes = [P, P, I32, I32, P, P, I64, P, P, P]
+    lib.moe_forward.argtypes = [P, P, I32, I32, P, P, P, I32, P]
+    lib.moe_layer_forward_routed.argtypes = [P, P, I32, I32, P, P, I64, P, P, P, I32, P]
+    lib.moe_residual_rmsnorm.argtypes = [P, P, I32, P, I32, I32, F, P]
+    lib.moe_layer_check.argtypes = [P]
+    lib.moe_layer_weight_bytes.argtypes = [P]
+    lib.moe_layer_weight_bytes.restype = I64
+    lib.moe_launch_count.argtypes = []
+    lib.moe_launch_count.restype = I64
+    lib.moe_status_string.argtypes = [I32]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_last_error.argtypes = []
+    lib.moe_last_error.restype = ctypes.c_char_p
+    for n in ("moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
+              "moe_layer_forward_routed", "moe_residual_rmsnorm", "moe_layer_check"):
+        getattr(lib, n).restype = I32
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        raise MoeError(status, load_library().moe_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return MOE_DT_BF16
+    if t.dtype == torch.float32:
+        return MOE_DT_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32")
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ---------------------------------------------------------------------------
+# Entry points (same names as the C ABI)
+# ---------------------------------------------------------------------------
+
+def moe_layer_create(hidden, n_experts, top_k, expert_ffn, n_shared, routed_scaling,
+                     max_tokens, up, gate, down, sh_up=None, sh_gate=None, sh_down=None,
+                     stream=None):
+    """Returns an opaque handle (int).  Weight tensors: uint8 on the GPU in
+    the IQ4_NL block layout of include/moe_gb300.h."""
+    lib = load_library()
+    sh = _Shapes(hidden, n_experts, top_k, expert_ffn, n_shared, routed_scaling, max_tokens, 0)
+    w = _Weights(*(_ptr(t) for t in (up, gate, down, sh_up, sh_gate, sh_down)))
+    out = ctypes.c_void_p()
+    _check(lib.moe_layer_create(ctypes.byref(sh), ctypes.byref(w), _stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def moe_layer_destroy(layer):
+    _check(load_library().moe_layer_destroy(ctypes.c_void_p(layer)))
+
+
+def moe_route(layer, x, router_w, ids, weights, logit_bias=None, bias_row_stride=None,
+              stream=None):
+    if bias_row_stride is None:
+        bias_row_stride = 0 if logit_bias is None or logit_bias.dim() == 1 else logit_bias.stride(0)
+    _check(load_library().moe_route(ctypes.c_void_p(layer), _ptr(x), _dtype(x), x.shape[0],
+                                    _ptr(router_w), _ptr(logit_bias), bias_row_stride,
+                                    _ptr(ids), _ptr(weights), _stream(stream)))
+
+
+def moe_forward(layer, x, ids, weights, out, stream=None):
+    _check(load_library().moe_forward(ctypes.c_void_p(layer), _ptr(x), _dtype(x), x.shape[0],
+                                      _ptr(ids), _ptr(weights), _ptr(out), _dtype(out),
+                                      _stream(stream)))
+
+
+def moe_layer_forward_routed(layer, x, router_w, ids, weights, out, logit_bias=None,
+                             bias_row_stride=None, stream=None):
+    if bias_row_stride is None:
+        bias_row_stride = 0 if logit_bias is None or logit_bias.dim() == 1 else logit_bias.stride(0)
+    _check(load_library().moe_layer_forward_routed(
+        ctypes.c_void_p(layer), _ptr(x), _dtype(x), x.shape[0], _ptr(router_w), _ptr(logit_bias),
+        bias_row_stride, _ptr(ids), _ptr(weights), _ptr(out), _dtype(out), _stream(stream)))
+
+
+def moe_residual_rmsnorm(resid, delta, u, eps, stream=None):
+    T, H = resid.shape
+    ddt = MOE_DT_FP32 if delta is None else _dtype(delta)
+    _check(load_library().moe_residual_rmsnorm(_ptr(resid), _ptr(delta), ddt, _ptr(u), T, H,
+                                               float(eps), _stream(stream)))
+
+
+def moe_layer_check(layer):
+    _check(load_library().moe_layer_check(ctypes.c_void_p(layer)))
+
+
+def moe_layer_weight_bytes(layer) -> int:
+    return int(load_library().moe_layer_weight_bytes(ctypes.c_void_p(layer)))
+
+
+def moe_launch_count() -> int:
+    return int(load_library().moe_launch_count())
+
+
+def moe_status_string(status: int) -> str:
+    return load_library().moe_status_string(status).decode()
+
+
+def moe_last_error() -> str:
+    return load_library().moe_last_error().decode(errors="replace")
+
+
+class MoeLayer:
+    """Owns one layer handle; keeps nothing else alive (the library copied
+    the weights).  Methods are the entry points with the handle bound."""
+
+    def __init__(self, hidden, n_experts, top_k, expert_ffn, n_shared=1, routed_scaling=2.0,
+                 max_tokens=1, *, up, gate, down, sh_up=None, sh_gate=None, sh_down=None,
+                 stream=None):
+        self.H, self.E, self.k, self.F, self.S = hidden, n_experts, top_k, expert_ffn, n_shared
+        self.scale, self.max_tokens = routed_scaling, max_tokens
+        self.handle = moe_layer_create(hidden, n_experts, top_k, expert_ffn, n_shared,
+                                       routed_scaling, max_tokens, up, gate, down, sh_up,
+                                       sh_gate, sh_down, stream)
+
+    @classmethod
+    def from_weights(cls, ew, k, scale=2.0, max_tokens=1, device="cuda", stream=None):
+        """Upload synth.ExpertWeights-like numpy arrays and create the layer."""
+        import torch
+        t = lambda a: None if a is None else torch.from_numpy(a).to(device)
+        E, F, nbh = ew.up.shape[0], ew.up.shape[1], ew.up.shape[2]
+        H = nbh * 32
+        S = 0 if getattr(ew, "sh_up", None) is None else 1
+        return cls(H, E, k, F, S, scale, max_tokens, up=t(ew.up), gate=t(ew.gate), down=t(ew.down),
+                   sh_up=t(ew.sh_up) if S else None, sh_gate=t(ew.sh_gate) if S else None,
+                   sh_down=t(ew.sh_down) if S else None, stream=stream)
+
+    def route(self, x, router_w, logit_bias=None, stream=None):
+        import torch
+        T = x.shape[0]
+        ids = torch.empty((T, self.k), dtype=torch.int32, device=x.device)
+        w = torch.empty((T, self.k), dtype=torch.float32, device=x.device)
+        moe_route(self.handle, x, router_w, ids, w, logit_bias, stream=stream)
+        return ids, w
+
+    def forward(self, x, ids, weights, out_dtype=None, stream=None):
+        import torch
+        out = torch.empty((x.shape[0], self.H), dtype=out_dtype or x.dtype, device=x.device)
+        moe_forward(self.handle, x, ids, weights, out, stream=stream)
+        return out
+
+    def forward_routed(self, x, router_w, logit_bias=None, out_dtype=None, stream=None):
+        import torch
+        T = x.shape[0]
+        ids = torch.empty((T, self.k), dtype=torch.int32, device=x.device)
+        w = torch.empty((T, self.k), dtype=torch.float32, device=x.device)
+        out = torch.empty((T, self.H), dtype=out_dtype or x.dtype, device=x.device)
+        moe_layer_forward_routed(self.handle, x, router_w, ids, w, out, logit_bias, stream=stream)
+        return out, ids, w
+
+    def check(self):
+        moe_layer_check(self.handle)
+
+    def weight_bytes(self):
+        return moe_layer_weight_bytes(self.handle)
+
+    def close(self):
+        if self.handle:
+            moe_layer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

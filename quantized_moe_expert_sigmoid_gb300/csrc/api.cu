@@ -1,0 +1,289 @@
+// C ABI of libmoe_gb300 (declared in include/moe_gb300.h).
+//
+// Failure policy (PocketLLM design record, section 5: refuse at load rather
+// than fail inside a request; EPQ model card, EPQ_REQUIRE_PAGER: fail loudly
+// instead of falling back): create validates the shape and allocates every
+// workspace for max_tokens up front; route and forward only validate their
+// arguments (including base-pointer alignment for vector loads) and launch.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <new>
+
+#include "moe_internal.cuh"
+
+using moe::Layer;
+
+namespace moe {
+static std::atomic<int64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace moe
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+moe_status fail(moe_status s, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+moe_status cuda_fail(cudaError_t e, const char *where) {
+  if (e == cudaErrorMemoryAllocation)
+    return fail(MOE_ERR_OUT_OF_MEMORY, "%s: %s", where, cudaGetErrorString(e));
+  return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+#define MOE_CUDA(call, where)                  \
+  do {                                         \
+    cudaError_t e_ = (call);                   \
+    if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+  } while (0)
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+bool is_device_ptr(const void *p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+void free_layer(Layer *L) {
+  if (!L) return;
+  void *ptrs[] = {L->gu, L->dn, L->logits, L->offsets, L->active, L->route_token,
+                  L->route_weight, L->h32, L->out_acc, L->err};
+  for (void *p : ptrs)
+    if (p) cudaFree(p);
+  delete L;
+}
+
+moe_status check_x(const Layer *L, const void *x, moe_dtype xdt, int32_t T) {
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d is negative", T);
+  if (T > L->max_tokens)
+    return fail(MOE_ERR_TOO_MANY_TOKENS, "T = %d exceeds max_tokens = %d", T, L->max_tokens);
+  if (xdt != MOE_DT_BF16 && xdt != MOE_DT_FP32)
+    return fail(MOE_ERR_INVALID_ARG, "x_dtype %d is not MOE_DT_BF16 or MOE_DT_FP32", (int)xdt);
+  if (T > 0 && !x) return fail(MOE_ERR_INVALID_ARG, "x is NULL");
+  if (T > 0 && !moe::aligned(x, 16)) return fail(MOE_ERR_MISALIGNED, "x is not 16-byte aligned");
+  return MOE_OK;
+}
+
+moe_status route_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const float *wr,
+                      const float *bias, int64_t bstride, int32_t *ids, float *w,
+                      cudaStream_t st) {
+  moe_status s = check_x(L, x, xdt, T);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!wr || !ids || !w) return fail(MOE_ERR_INVALID_ARG, "router_w, ids and weights must be non-NULL");
+  if (!moe::aligned(wr, 16)) return fail(MOE_ERR_MISALIGNED, "router_w is not 16-byte aligned");
+  if (!moe::aligned(ids, 4) || !moe::aligned(w, 4))
+    return fail(MOE_ERR_MISALIGNED, "ids/weights are not 4-byte aligned");
+  if (bias && bstride < 0) return fail(MOE_ERR_INVALID_ARG, "bias_row_stride is negative");
+  MOE_CUDA(moe::launch_router_logits(*L, x, xdt, T, wr, bias, bstride, L->logits, st), "router logits");
+  MOE_CUDA(moe::launch_router_topk(*L, L->logits, T, ids, w, st), "router top-k");
+  return MOE_OK;
+}
+
+moe_status forward_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const int32_t *ids,
+                        const float *w, void *out, moe_dtype odt, cudaStream_t st) {
+  moe_status s = check_x(L, x, xdt, T);
+  if (s != MOE_OK) return s;
+  if (odt != MOE_DT_BF16 && odt != MOE_DT_FP32)
+    return fail(MOE_ERR_INVALID_ARG, "out_dtype %d is not MOE_DT_BF16 or MOE_DT_FP32", (int)odt);
+  if (T == 0) return MOE_OK;
+  if (!ids || !w || !out) return fail(MOE_ERR_INVALID_ARG, "ids, weights and out must be non-NULL");
+  if (!moe::aligned(ids, 4) || !moe::aligned(w, 4))
+    return fail(MOE_ERR_MISALIGNED, "ids/weights are not 4-byte aligned");
+  if (!moe::aligned(out, 16)) return fail(MOE_ERR_MISALIGNED, "out is not 16-byte aligned");
+  MOE_CUDA(cudaMemsetAsync(L->out_acc, 0, sizeof(float) * (size_t)T * L->H, st), "clear accumulator");
+  MOE_CUDA(moe::launch_route_plan(*L, ids, w, T, st), "route plan");
+  MOE_CUDA(moe::launch_upgate_simt(*L, x, xdt, T, st), "up/gate");
+  MOE_CUDA(moe::launch_down_simt(*L, T, st), "down");
+  MOE_CUDA(moe::launch_finalize(*L, T, out, odt, st), "finalize");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+    case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED";
+    case MOE_ERR_OUT_OF_MEMORY: return "MOE_ERR_OUT_OF_MEMORY";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_BAD_EXPERT_ID: return "MOE_ERR_BAD_EXPERT_ID";
+    case MOE_ERR_TOO_MANY_TOKENS: return "MOE_ERR_TOO_MANY_TOKENS";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+const char *moe_last_error(void) { return g_err; }
+
+int64_t moe_launch_count(void) { return moe::g_launches.load(std::memory_order_relaxed); }
+
+moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *stream,
+                            moe_layer_t *out) {
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!sh || !wt) return fail(MOE_ERR_INVALID_ARG, "shapes and weights must be non-NULL");
+  const int H = sh->hidden, E = sh->n_experts, k = sh->top_k, F = sh->expert_ffn, S = sh->n_shared;
+  if (H < 32 || H > 16384 || H % 32) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "hidden = %d: need a multiple of 32 in [32, 16384]", H);
+  if (F < 32 || F > 16384 || F % 32) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "expert_ffn = %d: need a multiple of 32 in [32, 16384]", F);
+  if (E < 1 || E > 256) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "n_experts = %d: need 1..256", E);
+  if (k < 1 || k > 8 || k > E) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "top_k = %d: need 1..min(n_experts, 8)", k);
+  if (S != 0 && S != 1) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "n_shared = %d: need 0 or 1", S);
+  if (!(sh->routed_scaling > 0.f)) return fail(MOE_ERR_INVALID_ARG, "routed_scaling must be > 0");
+  if (sh->max_tokens < 1 || sh->max_tokens > 65536) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "max_tokens = %d: need 1..65536", sh->max_tokens);
+  if (sh->flags != 0) return fail(MOE_ERR_INVALID_ARG, "flags must be 0");
+  if (!wt->up || !wt->gate || !wt->down) return fail(MOE_ERR_INVALID_ARG, "up, gate and down must be non-NULL");
+  if (S && (!wt->sh_up || !wt->sh_gate || !wt->sh_down)) return fail(MOE_ERR_INVALID_ARG, "shared expert weights must be non-NULL when n_shared = 1");
+  const void *wps[] = {wt->up, wt->gate, wt->down, S ? wt->sh_up : wt->up,
+                       S ? wt->sh_gate : wt->up, S ? wt->sh_down : wt->up};
+  for (const void *p : wps)
+    if (!is_device_ptr(p)) return fail(MOE_ERR_INVALID_ARG, "expert weights must be device memory");
+
+  Layer *L = new (std::nothrow) Layer();
+  if (!L) return fail(MOE_ERR_OUT_OF_MEMORY, "host allocation failed");
+  L->H = H; L->E = E; L->k = k; L->F = F; L->S = S;
+  L->scale = sh->routed_scaling;
+  L->max_tokens = sh->max_tokens;
+  L->Hp = (int)round_up(H, moe::kSBW);
+  L->Fp = (int)round_up(F, moe::kSBW);
+  L->gu_row_bytes = (int64_t)(L->Hp / moe::kSBW) * moe::kSBBytes;
+  L->dn_row_bytes = (int64_t)(L->Fp / moe::kSBW) * moe::kSBBytes;
+  L->gu_expert_bytes = 2 * (int64_t)L->Fp * L->gu_row_bytes;
+  L->dn_expert_bytes = (int64_t)L->Hp * L->dn_row_bytes;
+  L->weight_bytes = (int64_t)(E + S) * 3 * F * (H / 32) * 18;
+  L->max_routes = sh->max_tokens * k + S * sh->max_tokens;
+  cudaStream_t st = (cudaStream_t)stream;
+
+#define ALLOC(ptr, bytes)                                                          \
+  do {                                                                             \
+    cudaError_t e_ = cudaMalloc((void **)&(ptr), (size_t)(bytes));                 \
+    if (e_ != cudaSuccess) { free_layer(L); return cuda_fail(e_, "cudaMalloc " #ptr); } \
+  } while (0)
+
+  const int64_t gu_total = (int64_t)(E + S) * L->gu_expert_bytes;
+  const int64_t dn_total = (int64_t)(E + S) * L->dn_expert_bytes;
+  ALLOC(L->gu, gu_total);
+  ALLOC(L->dn, dn_total);
+  ALLOC(L->logits, sizeof(float) * (int64_t)sh->max_tokens * E);
+  ALLOC(L->offsets, sizeof(int) * (E + S + 1));
+  ALLOC(L->active, sizeof(int) * (E + S + 1));
+  ALLOC(L->route_token, sizeof(int) * (int64_t)L->max_routes);
+  ALLOC(L->route_weight, sizeof(float) * (int64_t)L->max_routes);
+  ALLOC(L->h32, sizeof(float) * (int64_t)L->max_routes * L->Fp);
+  ALLOC(L->out_acc, sizeof(float) * (int64_t)sh->max_tokens * H);
+  ALLOC(L->err, sizeof(unsigned));
+#undef ALLOC
+
+  cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess) e = cudaMemsetAsync(L->gu, 0, (size_t)gu_total, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(L->dn, 0, (size_t)dn_total, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(L->err, 0, sizeof(unsigned), st);
+  const int64_t up_bytes = (int64_t)F * (H / 32) * 18;
+  const int64_t dn_bytes = (int64_t)H * (F / 32) * 18;
+  for (int x = 0; x < E + S && e == cudaSuccess; ++x) {
+    const bool shared = x == E;
+    const uint8_t *up = shared ? (const uint8_t *)wt->sh_up : (const uint8_t *)wt->up + x * up_bytes;
+    const uint8_t *gate = shared ? (const uint8_t *)wt->sh_gate : (const uint8_t *)wt->gate + x * up_bytes;
+    const uint8_t *down = shared ? (const uint8_t *)wt->sh_down : (const uint8_t *)wt->down + x * dn_bytes;
+    uint8_t *gu = L->gu + x * L->gu_expert_bytes;
+    uint8_t *dn = L->dn + x * L->dn_expert_bytes;
+    e = moe::launch_repack(gate, F, H, gu, L->gu_row_bytes, 2 * moe::kGroupRows, 0, st);
+    if (e == cudaSuccess)
+      e = moe::launch_repack(up, F, H, gu, L->gu_row_bytes, 2 * moe::kGroupRows, moe::kGroupRows, st);
+    if (e == cudaSuccess) e = moe::launch_repack(down, H, F, dn, L->dn_row_bytes, 0, 0, st);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    free_layer(L);
+    return cuda_fail(e, "moe_layer_create");
+  }
+  *out = reinterpret_cast<moe_layer_t>(L);
+  return MOE_OK;
+}
+
+moe_status moe_layer_destroy(moe_layer_t layer) {
+  if (!layer) return MOE_OK;
+  cudaDeviceSynchronize();
+  free_layer(reinterpret_cast<Layer *>(layer));
+  return MOE_OK;
+}
+
+moe_status moe_route(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
+                     const float *router_w, const float *logit_bias, int64_t bias_row_stride,
+                     int32_t *ids, float *weights, void *stream) {
+  return route_impl(reinterpret_cast<Layer *>(layer), x, x_dtype, T, router_w, logit_bias,
+                    bias_row_stride, ids, weights, (cudaStream_t)stream);
+}
+
+moe_status moe_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
+                       const int32_t *ids, const float *weights, void *out, moe_dtype out_dtype,
+                       void *stream) {
+  return forward_impl(reinterpret_cast<Layer *>(layer), x, x_dtype, T, ids, weights, out,
+                      out_dtype, (cudaStream_t)stream);
+}
+
+moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype x_dtype,
+                                    int32_t T, const float *router_w, const float *logit_bias,
+                                    int64_t bias_row_stride, int32_t *ids, float *weights,
+                                    void *out, moe_dtype out_dtype, void *stream) {
+  Layer *L = reinterpret_cast<Layer *>(layer);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (out_dtype != MOE_DT_BF16 && out_dtype != MOE_DT_FP32)
+    return fail(MOE_ERR_INVALID_ARG, "out_dtype %d is not MOE_DT_BF16 or MOE_DT_FP32", (int)out_dtype);
+  if (T > 0 && !out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+  if (T > 0 && out && !moe::aligned(out, 16)) return fail(MOE_ERR_MISALIGNED, "out is not 16-byte aligned");
+  moe_status s = route_impl(L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, ids, weights, st);
+  if (s != MOE_OK) return s;
+  return forward_impl(L, x, x_dtype, T, ids, weights, out, out_dtype, st);
+}
+
+moe_status moe_residual_rmsnorm(float *resid, const void *delta, moe_dtype delta_dtype, void *u,
+                                int32_t T, int32_t H, float eps, void *stream) {
+  if (T < 0 || H <= 0 || H % 8) return fail(MOE_ERR_INVALID_ARG, "need T >= 0 and H a positive multiple of 8");
+  if (delta_dtype != MOE_DT_BF16 && delta_dtype != MOE_DT_FP32)
+    return fail(MOE_ERR_INVALID_ARG, "delta_dtype %d is not MOE_DT_BF16 or MOE_DT_FP32", (int)delta_dtype);
+  if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
+  if (T == 0) return MOE_OK;
+  if (!resid || !u) return fail(MOE_ERR_INVALID_ARG, "resid and u must be non-NULL");
+  if (!moe::aligned(resid, 16) || !moe::aligned(u, 16) || (delta && !moe::aligned(delta, 16)))
+    return fail(MOE_ERR_MISALIGNED, "resid, delta and u must be 16-byte aligned");
+  MOE_CUDA(moe::launch_residual_rmsnorm(resid, delta, delta_dtype, u, T, H, eps, (cudaStream_t)stream),
+           "residual rmsnorm");
+  return MOE_OK;
+}
+
+moe_status moe_layer_check(moe_layer_t layer) {
+  Layer *L = reinterpret_cast<Layer *>(layer);
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+  MOE_CUDA(cudaDeviceSynchronize(), "moe_layer_check");
+  unsigned err = 0;
+  MOE_CUDA(cudaMemcpy(&err, L->err, sizeof(unsigned), cudaMemcpyDeviceToHost), "read error word");
+  MOE_CUDA(cudaMemset(L->err, 0, sizeof(unsigned)), "clear error word");
+  if (err & moe::kErrTimeout) return fail(MOE_ERR_TIMEOUT, "a bounded device wait gave up");
+  if (err & moe::kErrBadId) return fail(MOE_ERR_BAD_EXPERT_ID, "an expert id outside [0, E) reached moe_forward");
+  return MOE_OK;
+}
+
+int64_t moe_layer_weight_bytes(moe_layer_t layer) {
+  Layer *L = reinterpret_cast<Layer *>(layer);
+  return L ? L->weight_bytes : -1;
+}
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+// Internal declarations of libmoe_gb300: the layer object, the repacked
+// weight layout and the launchers each kernel file provides.
+//
+// Weight layout held by a layer ("SB rows"): a matrix W[N x K] of IQ4_NL
+// blocks is stored as N rows of K/256 superblocks of 144 bytes:
+//   bytes   0..15   the 8 fp16 scales of blocks 0..7 of the superblock
+//   bytes  16..143  8 x 16 bytes: block j's 32 four-bit indices, weight m of
+//                   the block in nibble m (byte m/2, low nibble when m even)
+// Same byte count as the 18-byte blocks (8 x 18 = 144).  A whole superblock
+// is one 16-byte-aligned unit, so a row segment can be fetched with 128-bit
+// or bulk (TMA) copies, and a 32-bit word holds 8 consecutive weights.
+// Rows of K not a multiple of 256 are padded with zero blocks (scale 0).
+//
+// Per expert the gate and up matrices are interleaved in groups of 64 rows:
+// row 128*g + r is gate row 64*g + r, row 128*g + 64 + r is up row 64*g + r.
+// A 128-row tile therefore holds gate and up for the same 64 outputs.
+// The shared expert is stored as expert index E.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_gb300.h"
+
+namespace moe {
+
+constexpr int kQK = 32;         // weights per IQ4_NL block
+constexpr int kSBW = 256;       // weights per superblock
+constexpr int kSBBytes = 144;   // bytes per superblock
+constexpr int kGroupRows = 64;  // gate/up interleave group
+
+// Sticky device error bits (Layer::err).
+constexpr unsigned kErrBadId = 1u;
+constexpr unsigned kErrTimeout = 2u;
+
+struct Layer {
+  // shape
+  int H, E, k, F, S;  // S = number of shared experts (0 or 1)
+  float scale;
+  int max_tokens;
+  int Hp, Fp;                // H and F padded to multiples of 256
+  int64_t gu_row_bytes;      // Hp/256 * 144
+  int64_t dn_row_bytes;      // Fp/256 * 144
+  int64_t gu_expert_bytes;   // 2*Fp rows
+  int64_t dn_expert_bytes;   // Hp rows
+  int64_t weight_bytes;      // IQ4_NL bytes of the unpadded matrices
+
+  // weights
+  uint8_t *gu = nullptr;     // [(E+S)][2*Fp][gu_row_bytes]
+  uint8_t *dn = nullptr;     // [(E+S)][Hp][dn_row_bytes]
+
+  // workspace (sized for max_tokens at create)
+  int max_routes = 0;        // max_tokens*k + S*max_tokens
+  float *logits = nullptr;   // [max_tokens][E]
+  int *offsets = nullptr;    // [E+S+1] segment starts in route order
+  int *active = nullptr;     // [E+S+1] ids of experts with routes; [E+S] = count
+  int *route_token = nullptr;   // [max_routes]
+  float *route_weight = nullptr; // [max_routes]
+  float *h32 = nullptr;      // [max_routes][Fp] SwiGLU output (fp32)
+  float *out_acc = nullptr;  // [max_tokens][H] fp32 accumulator
+  unsigned *err = nullptr;   // sticky device error word
+};
+
+// Launch counter behind moe_launch_count(); every launcher adds its kernels.
+void count_launches(int n);
+
+// Alignment helper.
+inline bool aligned(const void *p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// ---- launchers (each .cu file defines its own) ---------------------------
+
+// repack.cu: one IQ4_NL matrix [rows x K] (18-byte blocks, row-major) into
+// SB rows.  dst_row(r) = (r / 64) * row_group_stride + row_group_offset + r % 64
+// when row_group_stride > 0, else r.
+cudaError_t launch_repack(const uint8_t *src, int rows, int K, uint8_t *dst,
+                          int64_t dst_row_bytes, int row_group_stride,
+                          int row_group_offset, cudaStream_t stream);
+
+// router.cu
+cudaError_t launch_router_logits(const Layer &L, const void *x, moe_dtype xdt, int T,
+                                 const float *wr, const float *bias, int64_t bias_stride,
+                                 float *logits, cudaStream_t stream);
+cudaError_t launch_router_topk(const Layer &L, const float *logits, int T, int32_t *ids,
+                               float *weights, cudaStream_t stream);
+
+// plan.cu: histogram, prefix sum and stable permutation of the routes.
+cudaError_t launch_route_plan(const Layer &L, const int32_t *ids, const float *weights,
+                              int T, cudaStream_t stream);
+
+// expert_simt.cu: CUDA-core expert path (any T).
+cudaError_t launch_upgate_simt(const Layer &L, const void *x, moe_dtype xdt, int T,
+                               cudaStream_t stream);
+cudaError_t launch_down_simt(const Layer &L, int T, cudaStream_t stream);
+cudaError_t launch_finalize(const Layer &L, int T, void *out, moe_dtype odt,
+                            cudaStream_t stream);
+
+// norm.cu
+cudaError_t launch_residual_rmsnorm(float *resid, const void *delta, moe_dtype ddt,
+                                    void *u, int T, int H, float eps, cudaStream_t stream);
+
+}  // namespace moe

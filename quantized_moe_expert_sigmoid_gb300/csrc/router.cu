@@ -1,0 +1,235 @@
+// Sigmoid top-k router (HelloSun/xing4_0-29b-IQ4_NL_EPQ model card, "模型與路由":
+// expert_gating_func = sigmoid, expert_weights_norm = yes, expert_weights_scale
+// = 2.0, 4 of 64 experts; the router matrix ffn_gate_inp is fp32).
+//
+// Step 1 (logits): l[t][e] = x[t] . Wr[e] + b[t][e], fp32 accumulation.
+//   - small T: one warp per expert streams its Wr row once with 128-bit loads
+//     and serves every token (Wr is read from HBM exactly once);
+//   - large T: a 32-token x 64-expert register-tiled SIMT product through
+//     shared memory (Wr rows are reused by 32 tokens per tile).
+// Step 2 (selection): one warp per token; the k largest logits are taken in
+// descending order (sigmoid is monotone, so this is the order of the
+// scores), equal logits going to the lower id; s = 1/(1+e^-l) for the k
+// selected; w = scale * s / sum(s).
+#include <float.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+template <typename XT>
+__device__ __forceinline__ float4 load_x4(const XT *p);
+
+template <>
+__device__ __forceinline__ float4 load_x4<float>(const float *p) {
+  return *reinterpret_cast<const float4 *>(p);
+}
+
+template <>
+__device__ __forceinline__ float4 load_x4<__nv_bfloat16>(const __nv_bfloat16 *p) {
+  const uint2 v = *reinterpret_cast<const uint2 *>(p);
+  float4 r;
+  r.x = __uint_as_float(v.x << 16);
+  r.y = __uint_as_float(v.x & 0xFFFF0000u);
+  r.z = __uint_as_float(v.y << 16);
+  r.w = __uint_as_float(v.y & 0xFFFF0000u);
+  return r;
+}
+
+constexpr int kSmallTokens = 4;  // tokens per pass in the small-T kernel
+
+template <typename XT>
+__global__ void __launch_bounds__(256) router_logits_small(const XT *__restrict__ x, int T, int H,
+                                                           const float *__restrict__ wr, int E,
+                                                           const float *__restrict__ bias,
+                                                           int64_t bstride,
+                                                           float *__restrict__ logits) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  if (e >= E) return;
+  const float *w = wr + (int64_t)e * H;
+  for (int t0 = 0; t0 < T; t0 += kSmallTokens) {
+    float acc[kSmallTokens];
+#pragma unroll
+    for (int i = 0; i < kSmallTokens; ++i) acc[i] = 0.f;
+    for (int c = lane * 4; c < H; c += 128) {
+      const float4 wv = *reinterpret_cast<const float4 *>(w + c);
+#pragma unroll
+      for (int i = 0; i < kSmallTokens; ++i) {
+        if (t0 + i < T) {
+          const float4 xv = load_x4<XT>(x + (int64_t)(t0 + i) * H + c);
+          acc[i] = fmaf(xv.x, wv.x, acc[i]);
+          acc[i] = fmaf(xv.y, wv.y, acc[i]);
+          acc[i] = fmaf(xv.z, wv.z, acc[i]);
+          acc[i] = fmaf(xv.w, wv.w, acc[i]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kSmallTokens; ++i) {
+      float v = acc[i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0 && t0 + i < T) {
+        if (bias) v += bias[(int64_t)(t0 + i) * bstride + e];
+        logits[(int64_t)(t0 + i) * E + e] = v;
+      }
+    }
+  }
+}
+
+constexpr int kTM = 32, kTN = 64, kKC = 32;
+
+template <typename XT>
+__global__ void __launch_bounds__(256) router_logits_tiled(const XT *__restrict__ x, int T, int H,
+                                                           const float *__restrict__ wr, int E,
+                                                           const float *__restrict__ bias,
+                                                           int64_t bstride,
+                                                           float *__restrict__ logits) {
+  __shared__ float xs[kKC][kTM + 4];
+  __shared__ __align__(16) float ws[kKC][kTN + 4];
+  const int tid = threadIdx.x;
+  const int ty = tid >> 4, tx = tid & 15;  // 16 x 16 threads: 2 tokens x 4 experts each
+  const int t0 = blockIdx.x * kTM, e0 = blockIdx.y * kTN;
+  float acc[2][4] = {};
+  for (int k0 = 0; k0 < H; k0 += kKC) {
+    {  // x tile: 32 tokens x 32 k, 4 per thread
+      const int tt = tid >> 3, kk = (tid & 7) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t0 + tt < T) v = load_x4<XT>(x + (int64_t)(t0 + tt) * H + k0 + kk);
+      xs[kk + 0][tt] = v.x;
+      xs[kk + 1][tt] = v.y;
+      xs[kk + 2][tt] = v.z;
+      xs[kk + 3][tt] = v.w;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // Wr tile: 64 experts x 32 k, 8 per thread
+      const int ee = (tid >> 3) + 32 * h, kk = (tid & 7) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e0 + ee < E) v = *reinterpret_cast<const float4 *>(wr + (int64_t)(e0 + ee) * H + k0 + kk);
+      ws[kk + 0][ee] = v.x;
+      ws[kk + 1][ee] = v.y;
+      ws[kk + 2][ee] = v.z;
+      ws[kk + 3][ee] = v.w;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < kKC; ++kk) {
+      const float a0 = xs[kk][ty * 2], a1 = xs[kk][ty * 2 + 1];
+      const float4 b = *reinterpret_cast<const float4 *>(&ws[kk][tx * 4]);
+      acc[0][0] = fmaf(a0, b.x, acc[0][0]);
+      acc[0][1] = fmaf(a0, b.y, acc[0][1]);
+      acc[0][2] = fmaf(a0, b.z, acc[0][2]);
+      acc[0][3] = fmaf(a0, b.w, acc[0][3]);
+      acc[1][0] = fmaf(a1, b.x, acc[1][0]);
+      acc[1][1] = fmaf(a1, b.y, acc[1][1]);
+      acc[1][2] = fmaf(a1, b.z, acc[1][2]);
+      acc[1][3] = fmaf(a1, b.w, acc[1][3]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int t = t0 + ty * 2 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e >= E) continue;
+      float v = acc[i][j];
+      if (bias) v += bias[(int64_t)t * bstride + e];
+      logits[(int64_t)t * E + e] = v;
+    }
+  }
+}
+
+// One warp per token.  E <= 256: lane holds experts lane + 32*i, i < 8.
+__global__ void __launch_bounds__(256) router_topk_kernel(const float *__restrict__ logits, int T,
+                                                          int E, int k, float scale,
+                                                          int32_t *__restrict__ ids,
+                                                          float *__restrict__ weights) {
+  const int lane = threadIdx.x & 31;
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    float l = e < E ? logits[(int64_t)t * E + e] : -FLT_MAX;
+    v[i] = (l == l) ? l : -FLT_MAX;  // NaN never wins
+  }
+  unsigned taken = 0;
+  int my_id = 0;
+  float my_s = 0.f, ssum = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float best = -INFINITY;
+    int bid = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < bid))) {
+        best = v[i];
+        bid = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
+      if (ob > best || (ob == best && oid < bid)) {
+        best = ob;
+        bid = oid;
+      }
+    }
+    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+    const float s = 1.0f / (1.0f + expf(-best));
+    ssum += s;
+    if (lane == j) {
+      my_id = bid;
+      my_s = s;
+    }
+  }
+  if (lane < k) {
+    ids[(int64_t)t * k + lane] = my_id;
+    weights[(int64_t)t * k + lane] = scale * my_s / ssum;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits(const Layer &L, const void *x, moe_dtype xdt, int T,
+                                 const float *wr, const float *bias, int64_t bias_stride,
+                                 float *logits, cudaStream_t stream) {
+  if (T <= 16) {
+    dim3 grid((L.E + 7) / 8);
+    if (xdt == MOE_DT_BF16)
+      router_logits_small<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+          (const __nv_bfloat16 *)x, T, L.H, wr, L.E, bias, bias_stride, logits);
+    else
+      router_logits_small<float><<<grid, 256, 0, stream>>>((const float *)x, T, L.H, wr, L.E,
+                                                           bias, bias_stride, logits);
+  } else {
+    dim3 grid((T + kTM - 1) / kTM, (L.E + kTN - 1) / kTN);
+    if (xdt == MOE_DT_BF16)
+      router_logits_tiled<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+          (const __nv_bfloat16 *)x, T, L.H, wr, L.E, bias, bias_stride, logits);
+    else
+      router_logits_tiled<float><<<grid, 256, 0, stream>>>((const float *)x, T, L.H, wr, L.E,
+                                                           bias, bias_stride, logits);
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_topk(const Layer &L, const float *logits, int T, int32_t *ids,
+                               float *weights, cudaStream_t stream) {
+  const int warps_per_block = 8;
+  const int blocks = (T + warps_per_block - 1) / warps_per_block;
+  router_topk_kernel<<<blocks, 32 * warps_per_block, 0, stream>>>(logits, T, L.E, L.k, L.scale,
+                                                                  ids, weights);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

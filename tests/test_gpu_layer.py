@@ -1,0 +1,202 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Workloads (seeded, synthetic): the tiny layer (H 256, E 8, top-2, F 128,
+4 tokens, fp32 x), and the Xing4-shaped layer (H 3584, E 64, top-4, F 1024,
+one shared expert) at decode batch 1, batched decode 64 and a 4,096-token
+prefill with Zipf-skewed routing.  Routing ids must match bit for bit (the
+inputs keep every token's top-k+1 scores >= 1e-4 apart); outputs must meet
+the tolerance in tests/parity.py.  At 4,096 tokens the GPU computes every
+token and the oracle a sample of them.
+"""
+import functools
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+from oracle import cases
+from quantized_moe_expert_sigmoid_gb300 import MoeError, MoeLayer, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+WORKLOADS = ["tiny", "decode1", "decode64", "prefill4096"]
+
+
+@functools.lru_cache(maxsize=None)
+def _case(name):
+    wl = synth.WORKLOADS[name]
+    ew = parity.weights(0, 0, wl.E, wl.H, wl.F, wl.n_shared)
+    return cases.make_case(wl, ew=ew)
+
+
+@functools.lru_cache(maxsize=None)
+def _layer(E, H, F, k, max_tokens):
+    ew = parity.weights(0, 0, E, H, F, 1)
+    return MoeLayer.from_weights(ew, k=k, scale=2.0, max_tokens=max_tokens)
+
+
+def _layer_for(name):
+    wl = synth.WORKLOADS[name]
+    return _layer(wl.E, wl.H, wl.F, wl.k, 4096 if wl.H == 3584 else 64)
+
+
+def _dev_inputs(c):
+    x = torch.from_numpy(c.x.view(np.int16) if c.wl.x_dtype == "bf16" else c.x).cuda()
+    if c.wl.x_dtype == "bf16":
+        x = x.view(torch.bfloat16)
+    wr = torch.from_numpy(c.wr).cuda()
+    bias = None if c.bias is None else torch.from_numpy(c.bias).cuda()
+    return x, wr, bias
+
+
+def _sample(T):
+    if T <= 64:
+        return np.arange(T)
+    rng = np.random.default_rng(1)
+    return np.unique(np.concatenate([np.arange(8), np.arange(T - 8, T), rng.choice(T, 24, replace=False)]))
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_route_ids_bit_exact(name):
+    c = _case(name)
+    L = _layer_for(name)
+    x, wr, bias = _dev_inputs(c)
+    ids, w = L.route(x, wr, bias)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(ids.cpu().numpy(), c.ids)
+    np.testing.assert_allclose(w.cpu().numpy(), c.w, rtol=0, atol=2e-6)
+    assert np.allclose(w.cpu().numpy().sum(1), 2.0, atol=2e-6)
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_forward_fp32_matches_oracle(name):
+    c = _case(name)
+    L = _layer_for(name)
+    x, _, _ = _dev_inputs(c)
+    ids = torch.from_numpy(c.ids).cuda()
+    w32 = c.w.astype(np.float32)
+    out = L.forward(x, ids, torch.from_numpy(w32).cuda(), out_dtype=torch.float32)
+    L.check()
+    idx = _sample(c.wl.T)
+    ref = oracle.moe_forward(c.x64[idx], c.ids[idx], w32[idx].astype(np.float64), c.ew)
+    parity.assert_close_fp32(out.cpu().numpy()[idx], ref, name)
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_forward_routed_matches_oracle_layer(name):
+    c = _case(name)
+    L = _layer_for(name)
+    x, wr, bias = _dev_inputs(c)
+    out, ids, w = L.forward_routed(x, wr, bias)
+    L.check()
+    np.testing.assert_array_equal(ids.cpu().numpy(), c.ids)
+    idx = _sample(c.wl.T)
+    ref = oracle.moe_forward(c.x64[idx], c.ids[idx], c.w[idx], c.ew)
+    got = out.float().cpu().numpy()[idx]
+    if c.wl.x_dtype == "bf16":
+        parity.assert_close_bf16(got, ref, name)
+    else:
+        parity.assert_close_fp32(got, ref, name)
+
+
+RAGGED = [  # (H, E, k, F, T, n_shared): padding of H and F to 256, odd E, k = 1, no shared
+    (96, 7, 3, 64, 5, 1),
+    (160, 5, 1, 96, 33, 1),
+    (288, 16, 4, 320, 100, 0),
+    (512, 3, 3, 32, 17, 1),
+]
+
+
+@pytest.mark.parametrize("H,E,k,F,T,S", RAGGED)
+def test_ragged_shapes(H, E, k, F, T, S):
+    wl = synth.Workload("ragged", H, E, k, F, T, "bf16", 1.2 / H ** 0.5, n_shared=S)
+    ew = synth.expert_weights(11, 0, E, H, F, S)
+    if not S:
+        ew.sh_up = ew.sh_gate = ew.sh_down = None
+    c = cases.make_case(wl, seed=11, ew=ew)
+    L = MoeLayer.from_weights(ew, k=k, scale=2.0, max_tokens=T + 3)
+    x, wr, _ = _dev_inputs(c)
+    out, ids, w = L.forward_routed(x, wr, out_dtype=torch.float32)
+    L.check()
+    np.testing.assert_array_equal(ids.cpu().numpy(), c.ids)
+    ref = oracle.moe_forward(c.x64, c.ids, c.w, ew)
+    parity.assert_close_fp32(out.cpu().numpy(), ref, f"H{H} E{E} k{k} F{F} T{T}")
+    L.close()
+
+
+def test_empty_batch_launches_nothing():
+    L = _layer_for("tiny")
+    x = torch.zeros((0, 256), device="cuda")
+    wr = torch.zeros((8, 256), device="cuda")
+    out, ids, w = L.forward_routed(x, wr)
+    L.check()
+    assert out.shape == (0, 256) and ids.shape == (0, 2)
+
+
+def test_too_many_tokens_rejected():
+    L = _layer_for("tiny")
+    x = torch.zeros((65, 256), device="cuda")
+    wr = torch.zeros((8, 256), device="cuda")
+    with pytest.raises(MoeError) as e:
+        L.route(x, wr)
+    assert e.value.name == "MOE_ERR_TOO_MANY_TOKENS"
+
+
+def test_misaligned_base_pointer_rejected():
+    L = _layer_for("tiny")
+    buf = torch.zeros(4 * 256 + 1, device="cuda")
+    x = buf[1:].view(4, 256)  # 4-byte offset view: contiguous but not 16-byte aligned
+    wr = torch.zeros((8, 256), device="cuda")
+    with pytest.raises(MoeError) as e:
+        L.route(x, wr)
+    assert e.value.name == "MOE_ERR_MISALIGNED"
+
+
+def test_bad_expert_id_is_reported_and_dropped():
+    c = _case("tiny")
+    L = _layer_for("tiny")
+    x, _, _ = _dev_inputs(c)
+    ids = c.ids.copy()
+    ids[1, 0] = 8          # outside [0, 8)
+    ids[2, 1] = -1
+    w32 = c.w.astype(np.float32)
+    out = L.forward(x, torch.from_numpy(ids).cuda(), torch.from_numpy(w32).cuda(),
+                    out_dtype=torch.float32)
+    with pytest.raises(MoeError) as e:
+        L.check()
+    assert e.value.name == "MOE_ERR_BAD_EXPERT_ID"
+    L.check()  # the error word is cleared after being reported
+    keep_w = w32.astype(np.float64).copy()
+    keep_ids = ids.copy()
+    for t, j in ((1, 0), (2, 1)):
+        keep_w[t, j] = 0.0
+        keep_ids[t, j] = 0
+    ref = oracle.moe_forward(c.x64, keep_ids, keep_w, c.ew)
+    parity.assert_close_fp32(out.cpu().numpy(), ref, "dropped routes")
+
+
+def test_shared_bias_row_and_permuted_routes():
+    """A [E] bias row (stride 0) is added to every token; and listing the
+    same routes in another slot order gives the same output."""
+    c = _case("decode64")
+    L = _layer_for("decode64")
+    x, wr, _ = _dev_inputs(c)
+    row = np.zeros(64, np.float32)
+    row[5] = 3.0
+    ids, w = L.route(x, wr, torch.from_numpy(row).cuda())
+    ref_ids, ref_w, _ = oracle.route(c.x64, c.wr, 4, 2.0, row)
+    gap = oracle.min_topk_gap(c.logits + row[None, :].astype(np.float64), 4)
+    ok = gap >= 1e-4
+    np.testing.assert_array_equal(ids.cpu().numpy()[ok], ref_ids[ok])
+    perm = np.array([2, 0, 3, 1])
+    ids2 = torch.from_numpy(c.ids[:, perm].copy()).cuda()
+    w2 = torch.from_numpy(c.w[:, perm].astype(np.float32)).cuda()
+    out1 = L.forward(x, torch.from_numpy(c.ids).cuda(), torch.from_numpy(c.w.astype(np.float32)).cuda(),
+                     out_dtype=torch.float32)
+    out2 = L.forward(x, ids2, w2, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    a, b = out1.cpu().numpy(), out2.cpu().numpy()
+    assert np.abs(a - b).max() <= 1e-5 * np.abs(a).max()
