@@ -52,6 +52,21 @@ def parse():
     return p.parse_args()
 
 
+METRIC = "MoE-layer tokens/s (expert-weight HBM GB/s as fraction of GB300 peak)"
+
+
+def bench_config(args, wl, world):
+    T = wl.T
+    NL, NX, G, cfg = bench_config(args, wl, world)
+    G = max(1, min(args.graph_steps, args.steps))
+    return NL, NX, G, {
+        "workload": wl.name, "tokens_per_step": T, "hidden": wl.H, "experts": wl.E,
+        "top_k": wl.k, "expert_ffn": wl.F, "shared_experts": 1,
+        "parallelism": f"replicas x{world}",
+        "l2": f"rotating over {NL} resident layers and {NX} inputs (inputs larger than L2)",
+        "graph_steps": G}
+
+
 def algorithmic_bytes(T, distinct_experts):
     """HBM bytes one call must move at least: the selected experts' and the
     shared expert's IQ4_NL weights, the fp32 router, x in and out (bf16)."""
@@ -134,10 +149,11 @@ def run_reference(args, rank, world):
     wl = synth.WORKLOADS[args.workload]
     budget = 90.0
     r = cpu_baseline(args.workload, min(budget, 3.0 + 0.2 * (args.steps + args.warmup)))
-    line = {"impl": "reference", "metric": "MoE-layer tokens/s", "value": r["value"],
+    _, _, _, cfg = bench_config(args, wl, world)
+    line = {"impl": "reference", "metric": METRIC, "value": r["value"],
             "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "tokens_per_step": wl.T},
+            "data": "synthetic", "config": cfg,
             "ms_per_step": 1000.0 * wl.T / r["value"],
             "cpu_baseline": r,
             "e2e": {"value": r["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -159,8 +175,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     wl = synth.WORKLOADS[args.workload]
     T = wl.T
-    NL = args.layers if T < 64 else max(1, min(args.layers, 2))
-    NX = 64 if T < 64 else 2
+    NL, NX, G, cfg = bench_config(args, wl, world)
 
     layers, routers = [], []
     for l in range(NL):
@@ -174,7 +189,6 @@ def run_ours(args, rank, world, local_rank):
     xs_host = [synth.activations(100 + rank, "bench", T, wl.H, np.full(T, i)) for i in range(NX)]
     xs = [torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16) for a in xs_host]
     bias = torch.from_numpy(synth.zipf_logit_bias(7, T, wl.E)).to(dev) if wl.zipf else None
-    G = max(1, min(args.graph_steps, args.steps))
     outs = [torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev) for _ in range(G)]
     ids = [torch.empty((T, wl.k), dtype=torch.int32, device=dev) for _ in range(G)]
     wts = [torch.empty((T, wl.k), dtype=torch.float32, device=dev) for _ in range(G)]
@@ -286,16 +300,12 @@ def run_ours(args, rank, world, local_rank):
     achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
     tokens_per_s = world * T * steps / (ms / 1e3)
     line = {
-        "metric": "MoE-layer tokens/s (expert-weight HBM GB/s as fraction of GB300 peak)",
+        "metric": METRIC,
         "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in/out, IQ4_NL weights, fp32 accumulate",
         "data": "synthetic (seeded; random IQ4_NL weights of the Xing4 layer shapes)",
-        "config": {"workload": wl.name, "tokens_per_step": T, "hidden": wl.H, "experts": wl.E,
-                   "top_k": wl.k, "expert_ffn": wl.F, "shared_experts": 1,
-                   "parallelism": f"replicas x{world}",
-                   "l2": f"rotating over {NL} resident layers and {NX} inputs (inputs larger than L2)",
-                   "graph_steps": G},
+        "config": cfg,
         "us_per_layer": ms_per_step * 1e3,
         "expert_weight_gbs": expert_bytes / (ms_per_step * 1e-3) / 1e9,
         "expert_weight_frac_of_hbm_peak": expert_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
