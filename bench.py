@@ -57,7 +57,8 @@ METRIC = "MoE-layer tokens/s (expert-weight HBM GB/s as fraction of GB300 peak)"
 
 def bench_config(args, wl, world):
     T = wl.T
-    NL, NX, G, cfg = bench_config(args, wl, world)
+    NL = args.layers if T < 64 else max(1, min(args.layers, 2))
+    NX = 64 if T < 64 else 2
     G = max(1, min(args.graph_steps, args.steps))
     return NL, NX, G, {
         "workload": wl.name, "tokens_per_step": T, "hidden": wl.H, "experts": wl.E,
