@@ -92,8 +92,24 @@ def _check(status: int):
         raise MoeError(status, load_library().moe_last_error().decode(errors="replace"))
 
 
-def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+def _ptr(t, name="tensor", dtypes=None):
+    """Device pointer of a dense tensor; the C ABI takes dense row-major
+    arrays, so a strided view or a wrong dtype is refused here."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (row-major); got strides {tuple(t.stride())}")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
+    if t.numel() and not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dt():
+    import torch
+    return {"x": (torch.bfloat16, torch.float32), "f32": (torch.float32,),
+            "i32": (torch.int32,), "u8": (torch.uint8,)}
 
 
 def _dtype(t) -> int:
@@ -122,7 +138,9 @@ def moe_layer_create(hidden, n_experts, top_k, expert_ffn, n_shared, routed_scal
     the IQ4_NL block layout of include/moe_gb300.h."""
     lib = load_library()
     sh = _Shapes(hidden, n_experts, top_k, expert_ffn, n_shared, routed_scaling, max_tokens, 0)
-    w = _Weights(*(_ptr(t) for t in (up, gate, down, sh_up, sh_gate, sh_down)))
+    w = _Weights(*(_ptr(t, n, _dt()["u8"]) for t, n in ((up, "up"), (gate, "gate"), (down, "down"),
+                                                         (sh_up, "sh_up"), (sh_gate, "sh_gate"),
+                                                         (sh_down, "sh_down"))))
     out = ctypes.c_void_p()
     _check(lib.moe_layer_create(ctypes.byref(sh), ctypes.byref(w), _stream(stream), ctypes.byref(out)))
     return out.value
@@ -136,30 +154,50 @@ def moe_route(layer, x, router_w, ids, weights, logit_bias=None, bias_row_stride
               stream=None):
     if bias_row_stride is None:
         bias_row_stride = 0 if logit_bias is None or logit_bias.dim() == 1 else logit_bias.stride(0)
-    _check(load_library().moe_route(ctypes.c_void_p(layer), _ptr(x), _dtype(x), x.shape[0],
-                                    _ptr(router_w), _ptr(logit_bias), bias_row_stride,
-                                    _ptr(ids), _ptr(weights), _stream(stream)))
+    d = _dt()
+    if logit_bias is not None and logit_bias.dim() == 2 and logit_bias.stride(1) == 1 \
+            and bias_row_stride == logit_bias.stride(0):
+        bias_p = ctypes.c_void_p(logit_bias.data_ptr())  # row-strided [T][E] view is allowed
+    else:
+        bias_p = _ptr(logit_bias, "logit_bias", d["f32"])
+    _check(load_library().moe_route(ctypes.c_void_p(layer), _ptr(x, "x", d["x"]), _dtype(x),
+                                    x.shape[0], _ptr(router_w, "router_w", d["f32"]), bias_p,
+                                    bias_row_stride, _ptr(ids, "ids", d["i32"]),
+                                    _ptr(weights, "weights", d["f32"]), _stream(stream)))
 
 
 def moe_forward(layer, x, ids, weights, out, stream=None):
-    _check(load_library().moe_forward(ctypes.c_void_p(layer), _ptr(x), _dtype(x), x.shape[0],
-                                      _ptr(ids), _ptr(weights), _ptr(out), _dtype(out),
-                                      _stream(stream)))
+    d = _dt()
+    _check(load_library().moe_forward(ctypes.c_void_p(layer), _ptr(x, "x", d["x"]), _dtype(x),
+                                      x.shape[0], _ptr(ids, "ids", d["i32"]),
+                                      _ptr(weights, "weights", d["f32"]), _ptr(out, "out", d["x"]),
+                                      _dtype(out), _stream(stream)))
 
 
 def moe_layer_forward_routed(layer, x, router_w, ids, weights, out, logit_bias=None,
                              bias_row_stride=None, stream=None):
     if bias_row_stride is None:
         bias_row_stride = 0 if logit_bias is None or logit_bias.dim() == 1 else logit_bias.stride(0)
+    d = _dt()
+    if logit_bias is not None and logit_bias.dim() == 2 and logit_bias.stride(1) == 1 \
+            and bias_row_stride == logit_bias.stride(0):
+        bias_p = ctypes.c_void_p(logit_bias.data_ptr())
+    else:
+        bias_p = _ptr(logit_bias, "logit_bias", d["f32"])
     _check(load_library().moe_layer_forward_routed(
-        ctypes.c_void_p(layer), _ptr(x), _dtype(x), x.shape[0], _ptr(router_w), _ptr(logit_bias),
-        bias_row_stride, _ptr(ids), _ptr(weights), _ptr(out), _dtype(out), _stream(stream)))
+        ctypes.c_void_p(layer), _ptr(x, "x", d["x"]), _dtype(x), x.shape[0],
+        _ptr(router_w, "router_w", d["f32"]), bias_p, bias_row_stride,
+        _ptr(ids, "ids", d["i32"]), _ptr(weights, "weights", d["f32"]), _ptr(out, "out", d["x"]),
+        _dtype(out), _stream(stream)))
 
 
 def moe_residual_rmsnorm(resid, delta, u, eps, stream=None):
     T, H = resid.shape
     ddt = MOE_DT_FP32 if delta is None else _dtype(delta)
-    _check(load_library().moe_residual_rmsnorm(_ptr(resid), _ptr(delta), ddt, _ptr(u), T, H,
+    d = _dt()
+    _check(load_library().moe_residual_rmsnorm(_ptr(resid, "resid", d["f32"]),
+                                               _ptr(delta, "delta", d["x"]), ddt,
+                                               _ptr(u, "u", (d["x"][0],)), T, H,
                                                float(eps), _stream(stream)))
 
 

@@ -193,10 +193,24 @@ def test_shared_bias_row_and_permuted_routes():
     np.testing.assert_array_equal(ids.cpu().numpy()[ok], ref_ids[ok])
     perm = np.array([2, 0, 3, 1])
     ids2 = torch.from_numpy(c.ids[:, perm].copy()).cuda()
-    w2 = torch.from_numpy(c.w[:, perm].astype(np.float32)).cuda()
+    w2 = torch.from_numpy(np.ascontiguousarray(c.w[:, perm], dtype=np.float32)).cuda()
     out1 = L.forward(x, torch.from_numpy(c.ids).cuda(), torch.from_numpy(c.w.astype(np.float32)).cuda(),
                      out_dtype=torch.float32)
     out2 = L.forward(x, ids2, w2, out_dtype=torch.float32)
     torch.cuda.synchronize()
     a, b = out1.cpu().numpy(), out2.cpu().numpy()
     assert np.abs(a - b).max() <= 1e-5 * np.abs(a).max()
+
+
+def test_binding_refuses_strided_and_mistyped_tensors():
+    c = _case("tiny")
+    L = _layer_for("tiny")
+    x, wr, _ = _dev_inputs(c)
+    ids = torch.from_numpy(c.ids).cuda()
+    w_t = torch.from_numpy(np.asfortranarray(c.w.astype(np.float32))).cuda()  # column-major
+    with pytest.raises(ValueError):
+        L.forward(x, ids, w_t)
+    with pytest.raises(TypeError):
+        L.forward(x, ids.long(), torch.from_numpy(c.w.astype(np.float32)).cuda())
+    with pytest.raises(ValueError):
+        L.route(x.t().contiguous().t(), wr)
