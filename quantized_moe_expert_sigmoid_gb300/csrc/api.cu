@@ -59,7 +59,7 @@ bool is_device_ptr(const void *p) {
 void free_layer(Layer *L) {
   if (!L) return;
   void *ptrs[] = {L->gu, L->dn, L->logits, L->offsets, L->active, L->route_token,
-                  L->route_weight, L->h32, L->out_acc, L->err};
+                  L->route_weight, L->h32, L->out_acc, L->err, L->sync};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   delete L;
@@ -104,6 +104,12 @@ moe_status forward_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const
   if (!moe::aligned(ids, 4) || !moe::aligned(w, 4))
     return fail(MOE_ERR_MISALIGNED, "ids/weights are not 4-byte aligned");
   if (!moe::aligned(out, 16)) return fail(MOE_ERR_MISALIGNED, "out is not 16-byte aligned");
+  if (moe::fused_decode_supported(*L, T)) {
+    MOE_CUDA(moe::launch_decode_fused(*L, x, xdt, T, nullptr, nullptr, 0, ids, w, nullptr, nullptr,
+                                      out, odt, st),
+             "fused decode");
+    return MOE_OK;
+  }
   MOE_CUDA(cudaMemsetAsync(L->out_acc, 0, sizeof(float) * (size_t)T * L->H, st), "clear accumulator");
   MOE_CUDA(moe::launch_route_plan(*L, ids, w, T, st), "route plan");
   MOE_CUDA(moe::launch_upgate_simt(*L, x, xdt, T, st), "up/gate");
@@ -189,12 +195,14 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   ALLOC(L->h32, sizeof(float) * (int64_t)L->max_routes * L->Fp);
   ALLOC(L->out_acc, sizeof(float) * (int64_t)sh->max_tokens * H);
   ALLOC(L->err, sizeof(unsigned));
+  ALLOC(L->sync, 4 * sizeof(unsigned));
 #undef ALLOC
 
   cudaError_t e = cudaSuccess;
   if (e == cudaSuccess) e = cudaMemsetAsync(L->gu, 0, (size_t)gu_total, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(L->dn, 0, (size_t)dn_total, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(L->err, 0, sizeof(unsigned), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(L->sync, 0, 4 * sizeof(unsigned), st);
   const int64_t up_bytes = (int64_t)F * (H / 32) * 18;
   const int64_t dn_bytes = (int64_t)H * (F / 32) * 18;
   for (int x = 0; x < E + S && e == cudaSuccess; ++x) {
@@ -249,6 +257,19 @@ moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype 
     return fail(MOE_ERR_INVALID_ARG, "out_dtype %d is not MOE_DT_BF16 or MOE_DT_FP32", (int)out_dtype);
   if (T > 0 && !out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
   if (T > 0 && out && !moe::aligned(out, 16)) return fail(MOE_ERR_MISALIGNED, "out is not 16-byte aligned");
+  if (L && T > 0 && T <= L->max_tokens && moe::fused_decode_supported(*L, T)) {
+    moe_status s = check_x(L, x, x_dtype, T);
+    if (s != MOE_OK) return s;
+    if (!router_w || !ids || !weights) return fail(MOE_ERR_INVALID_ARG, "router_w, ids and weights must be non-NULL");
+    if (!moe::aligned(router_w, 16)) return fail(MOE_ERR_MISALIGNED, "router_w is not 16-byte aligned");
+    if (!moe::aligned(ids, 4) || !moe::aligned(weights, 4))
+      return fail(MOE_ERR_MISALIGNED, "ids/weights are not 4-byte aligned");
+    if (logit_bias && bias_row_stride < 0) return fail(MOE_ERR_INVALID_ARG, "bias_row_stride is negative");
+    MOE_CUDA(moe::launch_decode_fused(*L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, nullptr,
+                                      nullptr, ids, weights, out, out_dtype, st),
+             "fused decode");
+    return MOE_OK;
+  }
   moe_status s = route_impl(L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, ids, weights, st);
   if (s != MOE_OK) return s;
   return forward_impl(L, x, x_dtype, T, ids, weights, out, out_dtype, st);

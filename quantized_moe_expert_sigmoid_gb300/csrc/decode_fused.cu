@@ -1,0 +1,867 @@
+// Whole MoE layer in one launch for small batches (T <= 8 tokens): router,
+// top-k, route plan, dequantising up/gate + SwiGLU, down projection and the
+// weighted combine with the shared expert.
+//
+// Why one launch: at batch 1 the layer reads ~31.9 MB (4 routed experts +
+// the shared expert at 6,193,152 B each, plus the 917,504 B router), which
+// GB300's HBM3e delivers in under 5 us; a launch boundary costs about 1-2 us,
+// so the three dependent steps (route -> up/gate -> down) share one grid.
+// (PocketLLM "Xing4.0-29B-A4B: the design record", section 6: the decode
+// step there was launch-bound, with the card idle three quarters of the time.)
+//
+// Grid: one CTA per SM (its shared memory forces 1 CTA/SM).  Each CTA has
+// 16 consumer warps and one producer warp:
+//   producer  issues 1D bulk (TMA) copies of weight rows into a ring of
+//             32 KB shared-memory stages (full/empty mbarriers per stage);
+//             before the programmatic-dependent-launch wait it already
+//             fetches this CTA's slice of the shared expert's up/gate rows
+//             and its router row (weights are immutable); then it waits
+//             (bounded) for every router logit, selects the top-k of every
+//             token, builds the route plan and issues the routed experts'
+//             up/gate rows and this CTA's rows of every W_down.
+//   consumers stage x, compute the router logit of expert `blockIdx.x`,
+//             quantise x to 16-bit integers per 32-block (power-of-two
+//             scale), stream the up/gate items (warp w: gate row (w < 8) or
+//             up row of output f0 + w % 8; the two meet through a named
+//             barrier for SwiGLU and write h to global memory), wait
+//             (bounded) until every CTA has written its h, then own output
+//             rows [c*H/G, (c+1)*H/G): every consumer thread keeps fixed
+//             (row, 16-weight) units of W_down, accumulates them over all
+//             experts (route weight folded into the activation scale) and the
+//             rows are reduced once -- one writer per output, no atomics in
+//             global memory.
+// Dequantisation is in registers: byte-permute lookups of the 4-bit labels
+// (device_utils.cuh) and dp2a (16-bit x 8-bit products) into exact int32
+// sums per 16 weights, scaled by the weight block's fp16 scale times the
+// activation block's scale.
+#include <float.h>
+
+#include <algorithm>
+
+#include "device_utils.cuh"
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kStage = 32768;
+constexpr int kMaxStages = 8;
+constexpr int kMaxItems = 192;
+constexpr int kMaxSlots = kFusedMaxTokens * 9;  // T shared + T*k routed (k <= 8)
+constexpr int kMaxEx = kFusedMaxTokens * 8 + 2;
+constexpr int kMaxRowsCta = 32;
+constexpr int kUnits = 3;  // down-phase (row, 16-weight) units per consumer thread
+constexpr int kH4 = 4;     // float4 loads in flight per thread when gathering h
+constexpr uint32_t kPollLimit = 1u << 24;
+constexpr uint32_t kSpinLimit = 1u << 21;
+constexpr int kBarConsumers = 1;  // named barrier ids (0 is __syncthreads)
+constexpr int kBarPair0 = 2;      // 2..9: gate/up warp pairs
+
+struct Params {
+  Layer L;
+  const void *x;
+  int x_bf16, T;
+  const float *wr, *bias;
+  int64_t bstride;
+  const int32_t *ids_in;
+  const float *w_in;
+  int32_t *ids_out;
+  float *w_out;
+  void *out;
+  int out_bf16;
+  int nstage, fpi;
+  int wr_rows_smem;  // router rows held in the last ring stage (0: read from global)
+  int hq_cap;        // routes whose quantised h fit in shared memory at once
+  unsigned *sync;    // [0] router arrivals, [1] h arrivals, [2] exits
+};
+
+struct Item {
+  int16_t kind;  // 0: up/gate rows of `count` outputs from f0; 1: W_down rows [f0, f0 + count)
+  int16_t a;     // expert slot
+  int32_t f0, count;
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float load_x(const void *x, int bf16, int64_t i) {
+  if (bf16) return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(x)[i] << 16);
+  return reinterpret_cast<const float *>(x)[i];
+}
+
+// NP > 0: rows of Hp = NP * 512 weights (NP 16-weight positions per lane);
+// NPD > 0: W_down rows of Fp = NPD * 16 weights.  With both known at compile
+// time every shared-memory offset in the inner loops is a per-lane base plus
+// an immediate.  NP = NPD = 0: any shape, runtime loops.
+template <int TT, int NP, int NPD>
+__global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], wr_bar, plan_bar;
+  __shared__ Item items[kMaxItems];
+  __shared__ int n_items, n_shared_items, n_ex, status;
+  __shared__ int r_tok[kMaxSlots];
+  __shared__ float r_w[kMaxSlots];
+  __shared__ int ex_id[kMaxEx], ex_rs[kMaxEx + 1];
+  __shared__ int8_t rid[kMaxEx][kFusedMaxTokens];  // route of token t inside expert a, or -1
+  __shared__ int skey[kFusedMaxTokens * 8], sorted_id[kFusedMaxTokens * 8];
+  __shared__ int sel_id[kFusedMaxTokens][8];
+  __shared__ float sel_w[kFusedMaxTokens][8];
+  __shared__ float red[kConsumerWarps][TT];
+  __shared__ float up_part[2][8][TT];  // [item parity][output][route]
+  __shared__ float rowacc[kMaxRowsCta][TT];
+
+  const Layer &L = p.L;
+  const int T = p.T, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int Hp = L.Hp, Fp = L.Fp, H = L.H, E = L.E, S = L.S, K = L.k;
+  const int64_t rb = L.gu_row_bytes, db = L.dn_row_bytes;
+  const int nst = p.nstage, hb = Hp / 32, fb32 = Fp / 32;
+  uint8_t *ring = smem;
+  int16_t *xq = reinterpret_cast<int16_t *>(smem + (size_t)nst * kStage);
+  float *sx = reinterpret_cast<float *>(xq + (size_t)T * Hp);
+  int16_t *hq = reinterpret_cast<int16_t *>(sx + (size_t)T * hb);
+  float *shs = reinterpret_cast<float *>(hq + (size_t)p.hq_cap * Fp);
+  const int n0 = (int)((int64_t)c * H / G), n1 = (int)((int64_t)(c + 1) * H / G);
+  const int nrows = n1 - n0;
+  const bool do_route = p.ids_in == nullptr;
+
+  auto add_upgate = [&](int a, int fb, int fe) {  // thread-serial
+    int f = fb;
+    while (f < fe && n_items < kMaxItems) {
+      const int grp_end = (f / kGroupRows + 1) * kGroupRows;
+      const int cnt = min(min(fe, grp_end) - f, p.fpi);
+      items[n_items++] = Item{0, (int16_t)a, f, cnt};
+      f += cnt;
+    }
+  };
+
+  // ---- set-up ----
+  if (tid == 0) {
+    for (int s = 0; s < nst; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    mbar_init(&wr_bar, 1);
+    mbar_init(&plan_bar, 1);
+    fence_mbar_init();
+    n_items = 0;
+    n_ex = 0;
+    status = 0;
+    ex_rs[0] = 0;
+    if (S) {
+      ex_id[0] = E;
+      ex_rs[1] = T;
+      n_ex = 1;
+      for (int t = 0; t < T; ++t) {
+        r_tok[t] = t;
+        r_w[t] = 1.0f;
+        rid[0][t] = (int8_t)t;
+      }
+      add_upgate(0, (int)((int64_t)c * Fp / G), (int)((int64_t)(c + 1) * Fp / G));
+    }
+    n_shared_items = n_items;
+  }
+  __syncthreads();
+
+  if (warp == kProducerWarp) {
+    // =========================== producer warp ===========================
+    auto issue = [&](int i) {
+      const Item it = items[i];
+      const int s = i % nst;
+      uint8_t *dst = ring + (size_t)s * kStage;
+      const int eid = ex_id[it.a];
+      if (it.kind == 0) {
+        const uint8_t *base = L.gu + (int64_t)eid * L.gu_expert_bytes;
+        const int64_t grow = (int64_t)(it.f0 / kGroupRows) * (2 * kGroupRows) + it.f0 % kGroupRows;
+        const uint32_t bytes = (uint32_t)(it.count * rb);
+        mbar_arrive_expect_tx(&full_bar[s], 2 * bytes);
+        bulk_g2s(dst, base + grow * rb, bytes, &full_bar[s]);
+        bulk_g2s(dst + p.fpi * rb, base + (grow + kGroupRows) * rb, bytes, &full_bar[s]);
+      } else {
+        const uint8_t *base = L.dn + (int64_t)eid * L.dn_expert_bytes + (int64_t)it.f0 * db;
+        const uint32_t bytes = (uint32_t)(it.count * db);
+        mbar_arrive_expect_tx(&full_bar[s], bytes);
+        bulk_g2s(dst, base, bytes, &full_bar[s]);
+      }
+    };
+    int issued = 0;
+    if (lane == 0) {
+      for (; issued < n_shared_items && issued < nst; ++issued) issue(issued);
+      if (do_route && p.wr_rows_smem > 0) {  // router rows -> last stage (no shared item uses it)
+        int nr = 0;
+        for (int e = c; e < E; e += G) ++nr;
+        if (nr > 0) {
+          mbar_arrive_expect_tx(&wr_bar, (uint32_t)(nr * H * 4));
+          int r = 0;
+          for (int e = c; e < E; e += G, ++r)
+            bulk_g2s(ring + (size_t)(nst - 1) * kStage + (size_t)r * H * 4, p.wr + (int64_t)e * H,
+                     (uint32_t)(H * 4), &wr_bar);
+        }
+      }
+    }
+    if (do_route && p.wr_rows_smem == 0)
+      for (int e = c; e < E; e += G)
+        for (int i = lane * 32; i < H; i += 32 * 32) prefetch_l2(p.wr + (int64_t)e * H + i);
+    pdl_wait();
+
+    bool ok = true;
+    if (do_route) {
+      if (lane == 0) ok = spin_until_geq(&p.sync[0], (unsigned)min(E, G), kSpinLimit);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok && lane == 0) {
+        atomicOr(&status, 1);
+        atomicOr(L.err, kErrTimeout);
+      }
+    }
+    if (ok) {
+      // ---- top-k of every token (every CTA computes the same selection) ----
+      for (int t = 0; t < T; ++t) {
+        if (do_route) {
+          float v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i;
+            const float l = e < E ? __ldcg(&L.logits[(int64_t)t * E + e]) : -FLT_MAX;
+            v[i] = (l == l) ? l : -FLT_MAX;  // NaN never wins
+          }
+          unsigned taken = 0;
+          float ssum = 0.f, my_s = 0.f;
+          int my_id = 0;
+          for (int j = 0; j < K; ++j) {
+            float best = -INFINITY;
+            int bid = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int e = lane + 32 * i;
+              if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < bid))) {
+                best = v[i];
+                bid = e;
+              }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+              const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
+              if (ob > best || (ob == best && oid < bid)) {
+                best = ob;
+                bid = oid;
+              }
+            }
+            if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+            const float sg = 1.0f / (1.0f + expf(-best));
+            ssum += sg;
+            if (lane == j) {
+              my_id = bid;
+              my_s = sg;
+            }
+          }
+          if (lane < K) {
+            const float wgt = L.scale * my_s / ssum;
+            sel_id[t][lane] = my_id;
+            sel_w[t][lane] = wgt;
+            if (c == 0) {
+              p.ids_out[(int64_t)t * K + lane] = my_id;
+              p.w_out[(int64_t)t * K + lane] = wgt;
+            }
+          }
+        } else if (lane < K) {
+          const int id = p.ids_in[(int64_t)t * K + lane];
+          const bool valid = id >= 0 && id < E;
+          if (!valid && c == 0) atomicOr(L.err, kErrBadId);
+          sel_id[t][lane] = valid ? id : -1;
+          sel_w[t][lane] = p.w_in[(int64_t)t * K + lane];
+        }
+      }
+      __syncwarp();
+      // ---- route plan: routes sorted by (expert, token), by rank ----
+      const int R = T * K;
+      const int sb0 = S ? T : 0;
+      int key[2], tk[2], ids[2];
+      float wv[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = lane + 32 * h;
+        key[h] = 0x7fffffff;
+        tk[h] = 0;
+        ids[h] = -1;
+        wv[h] = 0.f;
+        if (r < R) {
+          tk[h] = r / K;
+          ids[h] = sel_id[tk[h]][r % K];
+          wv[h] = sel_w[tk[h]][r % K];
+          if (ids[h] >= 0) key[h] = ids[h] * 16 + tk[h];
+        }
+        skey[r] = key[h];
+      }
+      __syncwarp();
+      const unsigned v0 = __ballot_sync(0xffffffffu, key[0] != 0x7fffffff);
+      const unsigned v1 = __ballot_sync(0xffffffffu, key[1] != 0x7fffffff);
+      const int n_valid = __popc(v0) + __popc(v1);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (key[h] != 0x7fffffff) {
+          int rank = 0;
+          for (int m = 0; m < R; ++m) rank += skey[m] < key[h];
+          r_tok[sb0 + rank] = tk[h];
+          r_w[sb0 + rank] = wv[h];
+          sorted_id[rank] = ids[h];
+        }
+      }
+      __syncwarp();
+      bool st[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rk = lane + 32 * h;
+        st[h] = rk < n_valid && (rk == 0 || sorted_id[rk - 1] != sorted_id[rk]);
+      }
+      const unsigned b0 = __ballot_sync(0xffffffffu, st[0]);
+      const unsigned b1 = __ballot_sync(0xffffffffu, st[1]);
+      const unsigned le = (2u << lane) - 1u;  // lanes <= this one
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rk = lane + 32 * h;
+        if (rk < n_valid && st[h]) {
+          const int a = S - 1 + (h == 0 ? __popc(b0 & le) : __popc(b0) + __popc(b1 & le));
+          ex_id[a] = sorted_id[rk];
+          ex_rs[a] = sb0 + rk;
+        }
+      }
+      const int nex = S + __popc(b0) + __popc(b1);
+      if (lane == 0) {
+        n_ex = nex;
+        ex_rs[nex] = sb0 + n_valid;
+      }
+      __syncwarp();
+      for (int idx = lane; idx < (nex - S) * T; idx += 32) {  // route of token t in expert a
+        const int a = S + idx / T, t = idx % T;
+        int r = -1;
+        for (int sl = ex_rs[a]; sl < ex_rs[a + 1]; ++sl)
+          if (r_tok[sl] == t) r = sl - ex_rs[a];
+        rid[a][t] = (int8_t)r;
+      }
+      if (lane == 0) {  // this CTA's share of the routed up/gate rows, then its W_down rows
+        const int D = nex - S;
+        const int64_t N = (int64_t)D * Fp;
+        const int64_t fb = (int64_t)c * N / G, fe = (int64_t)(c + 1) * N / G;
+        for (int a = S; a < nex; ++a) {
+          const int64_t lo = (int64_t)(a - S) * Fp, hi = lo + Fp;
+          const int64_t q0 = max(fb, lo), q1 = min(fe, hi);
+          if (q0 < q1) add_upgate(a, (int)(q0 - lo), (int)(q1 - lo));
+        }
+        for (int a = 0; a < nex && n_items < kMaxItems; ++a)
+          items[n_items++] = Item{1, (int16_t)a, n0, nrows};
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&plan_bar);  // release: the tables above become visible to the waiters
+      for (int i = issued; i < n_items; ++i) {
+        const int s = i % nst;
+        if (i >= nst &&
+            !mbar_wait_bounded(&empty_bar[s], (uint32_t)((i / nst) - 1) & 1u, kPollLimit)) {
+          atomicOr(&status, 2);
+          break;
+        }
+        issue(i);
+      }
+    }
+  } else {
+    // =========================== consumer warps ===========================
+    const int ct = tid;  // 0 .. kConsumers-1
+    pdl_wait();  // x, workspace, outputs and the sync words may come from the previous grid
+    const bool x_staged = p.x_bf16 != 0;
+    if (x_staged) {  // one round of 16-byte loads into the xq region (row stride Hp)
+      const int h8 = H / 8, hp8 = Hp / 8;
+      for (int j0 = ct; j0 < T * hp8; j0 += 4 * kConsumers) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + u * kConsumers;
+          const int t = j / hp8, c8 = j % hp8;
+          v[u] = make_uint4(0, 0, 0, 0);
+          if (j < T * hp8 && c8 < h8) v[u] = reinterpret_cast<const uint4 *>(p.x)[(int64_t)t * h8 + c8];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + u * kConsumers;
+          if (j < T * hp8) reinterpret_cast<uint4 *>(xq)[j] = v[u];
+        }
+      }
+    }
+    named_sync(kBarConsumers, kConsumers);
+
+    // ---- router logit(s) of the experts this CTA owns ----
+    if (do_route && c < E) {
+      const float *wrow = reinterpret_cast<const float *>(ring + (size_t)(nst - 1) * kStage);
+      if (p.wr_rows_smem > 0 && !mbar_wait_bounded(&wr_bar, 0, kPollLimit)) atomicOr(&status, 2);
+      int r = 0;
+      for (int e = c; e < E; e += G, ++r) {
+        float acc[TT];
+#pragma unroll
+        for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+        const float *w = p.wr_rows_smem > 0 ? wrow + (size_t)r * H : p.wr + (int64_t)e * H;
+        const uint16_t *xs = reinterpret_cast<const uint16_t *>(xq);
+#pragma unroll 4
+        for (int i = ct; i < H; i += kConsumers) {
+          const float wv = w[i];
+#pragma unroll
+          for (int t = 0; t < TT; ++t)
+            if (t < T) {
+              const float xv = x_staged ? __uint_as_float((uint32_t)xs[(size_t)t * Hp + i] << 16)
+                                        : load_x(p.x, 0, (int64_t)t * H + i);
+              acc[t] = fmaf(xv, wv, acc[t]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          const float v = warp_sum(acc[t]);
+          if (lane == 0) red[warp][t] = v;
+        }
+        named_sync(kBarConsumers, kConsumers);
+        if (ct < T) {
+          float v = 0.f;
+          for (int w2 = 0; w2 < kConsumerWarps; ++w2) v += red[w2][ct];
+          if (p.bias) v += p.bias[(int64_t)ct * p.bstride + e];
+          L.logits[(int64_t)ct * E + e] = v;
+        }
+        named_sync(kBarConsumers, kConsumers);
+      }
+      if (ct == 0) {
+        __threadfence();
+        atomicAdd(&p.sync[0], 1u);
+      }
+    }
+    named_sync(kBarConsumers, kConsumers);  // router done with the raw x
+
+    // ---- quantise x: one thread per 32-element block, in place ----
+    for (int idx = ct; idx < T * hb; idx += kConsumers) {
+      const int t = idx / hb, b = idx % hb;
+      float v[32];
+      if (x_staged) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(xq + (size_t)t * Hp + b * 32);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 w = src[k];
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            v[8 * k + 2 * m] = __uint_as_float(ww[m] << 16);
+            v[8 * k + 2 * m + 1] = __uint_as_float(ww[m] & 0xFFFF0000u);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int col = b * 32 + k;
+          v[k] = col < H ? load_x(p.x, 0, (int64_t)t * H + col) : 0.f;
+        }
+      }
+      float m = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) m = fmaxf(m, fabsf(v[k]));
+      const float sc = act_block_scale(m);
+      const float inv = __uint_as_float((uint32_t)(254u << 23) - __float_as_uint(sc));
+      uint32_t packed[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int q0 = max(-32767, min(32767, __float2int_rn(v[2 * k] * inv)));
+        const int q1 = max(-32767, min(32767, __float2int_rn(v[2 * k + 1] * inv)));
+        packed[k] = (uint32_t)(q0 & 0xFFFF) | ((uint32_t)q1 << 16);
+      }
+      uint4 *dst = reinterpret_cast<uint4 *>(xq + (size_t)t * Hp + b * 32);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        dst[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+      sx[(size_t)t * hb + b] = sc;
+    }
+    named_sync(kBarConsumers, kConsumers);
+
+    // One up/gate item: warp w works on output f0 + (w & 7), on its gate row
+    // (w < 8) or its up row (w >= 8); lanes split the row's 16-weight
+    // half-blocks.  The pair meets at a named barrier for SwiGLU.
+    auto process_upgate = [&](int i) {
+      const Item it = items[i];
+      const int s = i % nst;
+      if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(i / nst) & 1u, kPollLimit)) atomicOr(&status, 2);
+      const int rs = ex_rs[it.a], nr = ex_rs[it.a + 1] - rs;
+      const int fl = warp & 7, is_up = warp >> 3;
+      float acc[TT];
+#pragma unroll
+      for (int r = 0; r < TT; ++r) acc[r] = 0.f;
+      if (fl < it.count) {
+        const uint8_t *row = ring + (size_t)s * kStage + (size_t)(is_up * p.fpi + fl) * rb;
+        int toks[TT];
+#pragma unroll
+        for (int r = 0; r < TT; ++r) toks[r] = r < nr ? r_tok[rs + r] : 0;
+        if constexpr (NP > 0) {
+          constexpr int kHp = NP * 512, kHb = NP * 16;
+          const uint8_t *wl = row + (lane >> 4) * kSBBytes + 16 + ((lane >> 1) & 7) * 16 + (lane & 1) * 8;
+          const uint8_t *dl = row + (lane >> 4) * kSBBytes + ((lane >> 1) & 7) * 2;
+          const int b0 = lane >> 1;
+#pragma unroll
+          for (int k = 0; k < NP; ++k) {
+            const uint2 q = *reinterpret_cast<const uint2 *>(wl + 2 * kSBBytes * k);
+            const float d = __half2float(*reinterpret_cast<const __half *>(dl + 2 * kSBBytes * k));
+            uint32_t c0, c1, c2, c3;
+            iq4_decode8(q.x, c0, c1);
+            iq4_decode8(q.y, c2, c3);
+#pragma unroll
+            for (int r = 0; r < TT; ++r) {
+              if (r < nr) {
+                const int16_t *xr = xq + toks[r] * kHp + lane * 16 + 512 * k;
+                const uint4 xa = *reinterpret_cast<const uint4 *>(xr);
+                const uint4 xb = *reinterpret_cast<const uint4 *>(xr + 8);
+                const int s0 = dot8_dp2a(c0, c1, xa, 0);
+                const int s1 = dot8_dp2a(c2, c3, xb, 0);
+                acc[r] = fmaf((float)(s0 + s1), d * sx[toks[r] * kHb + b0 + 16 * k], acc[r]);
+              }
+            }
+          }
+        } else {
+#pragma unroll 2
+          for (int pos = lane; pos < Hp / 16; pos += 32) {
+            const int b = pos >> 1, sb = b >> 3, j = b & 7, half = pos & 1;
+            const uint8_t *ps = row + sb * kSBBytes;
+            const float d = __half2float(reinterpret_cast<const __half *>(ps)[j]);
+            const uint2 q = *reinterpret_cast<const uint2 *>(ps + 16 + j * 16 + half * 8);
+            uint32_t c0, c1, c2, c3;
+            iq4_decode8(q.x, c0, c1);
+            iq4_decode8(q.y, c2, c3);
+#pragma unroll
+            for (int r = 0; r < TT; ++r) {
+              if (r < nr) {
+                const uint4 *xp4 = reinterpret_cast<const uint4 *>(xq + (size_t)toks[r] * Hp + pos * 16);
+                const uint4 xa = xp4[0], xb = xp4[1];
+                const int s0 = dot8_dp2a(c0, c1, xa, 0);
+                const int s1 = dot8_dp2a(c2, c3, xb, 0);
+                acc[r] = fmaf((float)(s0 + s1), d * sx[(size_t)toks[r] * hb + b], acc[r]);
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);  // this warp is done with the stage
+      if (fl < it.count) {
+        float v[TT];
+#pragma unroll
+        for (int r = 0; r < TT; ++r) v[r] = r < nr ? warp_sum(acc[r]) : 0.f;
+        if (is_up && lane == 0)
+          for (int r = 0; r < nr; ++r) up_part[i & 1][fl][r] = v[r];
+        named_sync(kBarPair0 + fl, 64);
+        if (!is_up && lane == 0)
+          for (int r = 0; r < nr; ++r) {
+            const float g = v[r], u = up_part[i & 1][fl][r];
+            L.h32[(int64_t)(rs + r) * Fp + it.f0 + fl] = g / (1.0f + expf(-g)) * u;
+          }
+      }
+    };
+
+    int i = 0;
+    for (; i < n_shared_items; ++i) process_upgate(i);
+    if (!mbar_wait_bounded(&plan_bar, 0, kPollLimit)) atomicOr(&status, 2);
+    if (!(status & 1)) {
+      for (; i < n_items && items[i].kind == 0; ++i) process_upgate(i);
+
+      // ---- every CTA's h written ----
+      named_sync(kBarConsumers, kConsumers);
+      if (ct == 0) {
+        __threadfence();
+        atomicAdd(&p.sync[1], 1u);
+        if (!spin_until_geq(&p.sync[1], (unsigned)G, kSpinLimit)) {
+          atomicOr(&status, 1);
+          atomicOr(L.err, kErrTimeout);
+        }
+      }
+      named_sync(kBarConsumers, kConsumers);
+      pdl_launch_dependents();
+
+      // ---- W_down rows of this CTA, summed over all experts ----
+      const int npd = Fp / 16;  // 16-weight units per row
+      float acc[kUnits][TT];
+#pragma unroll
+      for (int m = 0; m < kUnits; ++m)
+#pragma unroll
+        for (int t = 0; t < TT; ++t) acc[m][t] = 0.f;
+      for (int idx = ct; idx < kMaxRowsCta * TT; idx += kConsumers) (&rowacc[0][0])[idx] = 0.f;
+      int grp_end = -1, grp_rs = 0;  // experts [.., grp_end) have their h in hq
+      for (; i < n_items; ++i) {
+        const Item it = items[i];
+        const int a = it.a;
+        const int rs = ex_rs[a];
+        if (a >= grp_end) {
+          // next group of whole experts that fits hq; all its loads are issued
+          // before any is used (one round trip to L2)
+          if (grp_end >= 0) named_sync(kBarConsumers, kConsumers);  // previous group no longer read
+          int ge = a + 1;
+          while (ge < n_ex && ex_rs[ge + 1] - rs <= p.hq_cap) ++ge;
+          const int f4 = Fp / 4;
+          const int total4 = (ex_rs[ge] - rs) * f4;
+          const float4 *src = reinterpret_cast<const float4 *>(L.h32 + (int64_t)rs * Fp);
+          for (int base = 0; base < total4; base += kConsumers * kH4) {
+            float4 v[kH4];
+#pragma unroll
+            for (int m = 0; m < kH4; ++m) {
+              const int j = base + ct + m * kConsumers;
+              v[m] = j < total4 ? __ldcg(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int m = 0; m < kH4; ++m) {
+              const int j = base + ct + m * kConsumers;  // 8 consecutive j: one 32-block
+              float mx = fmaxf(fmaxf(fabsf(v[m].x), fabsf(v[m].y)), fmaxf(fabsf(v[m].z), fabsf(v[m].w)));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              if (j < total4) {
+                const float sc = act_block_scale(mx);
+                const float inv = __uint_as_float((uint32_t)(254u << 23) - __float_as_uint(sc));
+                const int q0 = max(-32767, min(32767, __float2int_rn(v[m].x * inv)));
+                const int q1 = max(-32767, min(32767, __float2int_rn(v[m].y * inv)));
+                const int q2 = max(-32767, min(32767, __float2int_rn(v[m].z * inv)));
+                const int q3 = max(-32767, min(32767, __float2int_rn(v[m].w * inv)));
+                reinterpret_cast<uint2 *>(hq)[j] =
+                    make_uint2((uint32_t)(q0 & 0xFFFF) | ((uint32_t)q1 << 16),
+                               (uint32_t)(q2 & 0xFFFF) | ((uint32_t)q3 << 16));
+                if ((ct & 7) == 0) shs[j / 8] = sc * r_w[rs + j / f4];  // route weight folded in
+              }
+            }
+          }
+          grp_end = ge;
+          grp_rs = rs;
+          named_sync(kBarConsumers, kConsumers);
+        }
+        const int hoff = rs - grp_rs;
+        const int s = i % nst;
+        if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(i / nst) & 1u, kPollLimit)) atomicOr(&status, 2);
+        int rids[TT];
+#pragma unroll
+        for (int t = 0; t < TT; ++t) rids[t] = t < T ? (int)rid[a][t] : -1;
+        if constexpr (NPD > 0) {
+          constexpr int kFp = NPD * 16, kDb = NPD / 16 * kSBBytes, kRowStep = kConsumers / NPD;
+          static_assert(kConsumers % NPD == 0, "units of a thread share one position");
+          const int pos = ct & (NPD - 1), b = pos >> 1;
+          const int wofs = (b >> 3) * kSBBytes + 16 + (b & 7) * 16 + (pos & 1) * 8;
+          const int dofs = (b >> 3) * kSBBytes + (b & 7) * 2;
+          const uint8_t *st = ring + (size_t)s * kStage + (ct / NPD) * kDb;
+#pragma unroll
+          for (int m = 0; m < kUnits; ++m) {
+            const int rr = ct / NPD + kRowStep * m;
+            if (rr < it.count) {
+              const uint2 q = *reinterpret_cast<const uint2 *>(st + kRowStep * kDb * m + wofs);
+              const float d = __half2float(*reinterpret_cast<const __half *>(st + kRowStep * kDb * m + dofs));
+              uint32_t c0, c1, c2, c3;
+              iq4_decode8(q.x, c0, c1);
+              iq4_decode8(q.y, c2, c3);
+#pragma unroll
+              for (int t = 0; t < TT; ++t) {
+                const int r = rids[t];
+                if (r >= 0) {
+                  const int16_t *hr = hq + (hoff + r) * kFp + pos * 16;
+                  const uint4 ha = *reinterpret_cast<const uint4 *>(hr);
+                  const uint4 hb2 = *reinterpret_cast<const uint4 *>(hr + 8);
+                  const int s0 = dot8_dp2a(c0, c1, ha, 0);
+                  const int s1 = dot8_dp2a(c2, c3, hb2, 0);
+                  acc[m][t] = fmaf((float)(s0 + s1), d * shs[(hoff + r) * (kFp / 32) + b], acc[m][t]);
+                }
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int m = 0; m < kUnits; ++m) {
+            const int u = ct + kConsumers * m;
+            const int rr = u / npd, pos = u % npd;
+            if (rr < it.count) {
+              const int b = pos >> 1, sb = b >> 3, j = b & 7, half = pos & 1;
+              const uint8_t *ps = ring + (size_t)s * kStage + (size_t)rr * db + sb * kSBBytes;
+              const float d = __half2float(reinterpret_cast<const __half *>(ps)[j]);
+              const uint2 q = *reinterpret_cast<const uint2 *>(ps + 16 + j * 16 + half * 8);
+              uint32_t c0, c1, c2, c3;
+              iq4_decode8(q.x, c0, c1);
+              iq4_decode8(q.y, c2, c3);
+#pragma unroll
+              for (int t = 0; t < TT; ++t) {
+                const int r = rids[t];
+                if (r >= 0) {
+                  const uint4 *hp4 =
+                      reinterpret_cast<const uint4 *>(hq + (size_t)(hoff + r) * Fp + pos * 16);
+                  const uint4 ha = hp4[0], hb2 = hp4[1];
+                  const int s0 = dot8_dp2a(c0, c1, ha, 0);
+                  const int s1 = dot8_dp2a(c2, c3, hb2, 0);
+                  acc[m][t] = fmaf((float)(s0 + s1), d * shs[(size_t)(hoff + r) * fb32 + b], acc[m][t]);
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+      }
+      // ---- reduce the units of each row and write the owned output rows ----
+#pragma unroll
+      for (int m = 0; m < kUnits; ++m) {
+        const int u = ct + kConsumers * m;
+        const int rr = u / npd;
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          if (t < T) {
+            if ((npd & 31) == 0) {  // a warp's 32 units lie in one row
+              const float v = warp_sum(acc[m][t]);
+              if (lane == 0 && rr < nrows) atomicAdd(&rowacc[rr][t], v);
+            } else if (rr < nrows) {
+              atomicAdd(&rowacc[rr][t], acc[m][t]);
+            }
+          }
+        }
+      }
+      named_sync(kBarConsumers, kConsumers);
+      for (int idx = ct; idx < nrows * T; idx += kConsumers) {
+        const int t = idx / nrows, rr = idx % nrows;
+        const float v = rowacc[rr][t];
+        const int64_t o = (int64_t)t * H + n0 + rr;
+        if (p.out_bf16)
+          reinterpret_cast<__nv_bfloat16 *>(p.out)[o] = __float2bfloat16_rn(v);
+        else
+          reinterpret_cast<float *>(p.out)[o] = v;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (tid == 0) {
+    if (status & 2) atomicOr(L.err, kErrTimeout);
+    __threadfence();
+    const unsigned v = atomicAdd(&p.sync[2], 1u);
+    if (v == (unsigned)G - 1) {  // last CTA out resets the words for the next call
+      p.sync[0] = 0;
+      p.sync[1] = 0;
+      p.sync[2] = 0;
+      __threadfence();
+    }
+  }
+}
+
+int g_sms = 0;
+
+struct FusedPlan {
+  int fpi, nstage, hq_cap, wr_rows_smem;
+  size_t smem;
+};
+
+// Shared-memory plan for T tokens; false if the layer does not fit the
+// single-launch kernel.
+bool plan_fused(const Layer &L, int T, FusedPlan &fp) {
+  if (T < 1 || T > kFusedMaxTokens || L.k > 8 || L.E > 256) return false;
+  if (g_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+  }
+  fp.fpi = (int)std::min<int64_t>(8, kStage / (2 * L.gu_row_bytes));
+  if (fp.fpi < 1) return false;
+  const int rows_cta = (L.H + g_sms - 1) / g_sms;
+  if (rows_cta > kMaxRowsCta || (int64_t)rows_cta * L.dn_row_bytes > kStage) return false;
+  if ((int64_t)rows_cta * (L.Fp / 16) > (int64_t)kUnits * kConsumers) return false;
+  const size_t per_route = (size_t)L.Fp * 2 + (size_t)(L.Fp / 32) * 4;
+  const size_t fixed = (size_t)T * L.Hp * 2 + (size_t)T * (L.Hp / 32) * 4;
+  const size_t limit = smem_limit_fused();
+  if (fixed + (size_t)T * per_route + 3 * (size_t)kStage > limit) return false;
+  fp.nstage = (int)std::min<size_t>(kMaxStages, (limit - fixed - (size_t)T * per_route) / kStage);
+  const size_t left = limit - fixed - (size_t)fp.nstage * kStage;
+  fp.hq_cap = (int)std::min<size_t>((size_t)T * (L.k + L.S), left / per_route);
+  fp.smem = fixed + (size_t)fp.nstage * kStage + (size_t)fp.hq_cap * per_route;
+  // router rows in the last stage when they fit and no shared item uses it
+  const int router_rows = (L.E + g_sms - 1) / g_sms;
+  const int64_t f_sh = L.Fp / g_sms + 1;
+  const int shared_items = (int)(f_sh / fp.fpi + 2 + f_sh / kGroupRows);
+  fp.wr_rows_smem = ((int64_t)router_rows * L.H * 4 <= kStage && shared_items <= fp.nstage - 1)
+                        ? router_rows : 0;
+  // item-count bound: shared + routed up/gate + one W_down item per expert
+  const int64_t D = std::min<int64_t>((int64_t)T * L.k, L.E);
+  const int64_t f_rt = D * L.Fp / g_sms + 1;
+  const int64_t items = shared_items + (f_rt / fp.fpi + D + f_rt / kGroupRows + 2) + (D + L.S);
+  return items <= kMaxItems;
+}
+
+template <int TT, int NP, int NPD>
+cudaError_t launch_tt(const Params &p, size_t smem, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<TT, NP, NPD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_limit_fused());
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_fused_kernel<TT, NP, NPD>, p);
+}
+
+}  // namespace
+
+size_t smem_limit_fused() { return 232448 - 8192; }  // dynamic part; static tables take < 8 KB
+
+bool fused_decode_supported(const Layer &L, int T) {
+  FusedPlan fp;
+  return plan_fused(L, T, fp);
+}
+
+cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, int T,
+                                const float *wr, const float *bias, int64_t bstride,
+                                const int32_t *ids_in, const float *w_in, int32_t *ids_out,
+                                float *w_out, void *out, moe_dtype odt, cudaStream_t stream) {
+  FusedPlan fp;
+  if (!plan_fused(L, T, fp)) return cudaErrorInvalidConfiguration;
+  Params p;
+  p.L = L;
+  p.x = x;
+  p.x_bf16 = xdt == MOE_DT_BF16;
+  p.T = T;
+  p.wr = wr;
+  p.bias = bias;
+  p.bstride = bstride;
+  p.ids_in = ids_in;
+  p.w_in = w_in;
+  p.ids_out = ids_out;
+  p.w_out = w_out;
+  p.out = out;
+  p.out_bf16 = odt == MOE_DT_BF16;
+  p.nstage = fp.nstage;
+  p.fpi = fp.fpi;
+  p.hq_cap = fp.hq_cap;
+  p.wr_rows_smem = fp.wr_rows_smem;
+  p.sync = L.sync;
+  cudaError_t e;
+  // compile-time shape for the Xing4 layer (H 3584, F 1024); any other shape
+  // takes the runtime-loop instance
+  const bool xing4 = L.Hp == 3584 && L.Fp == 1024;
+  if (T <= 1)
+    e = xing4 ? launch_tt<1, 7, 64>(p, fp.smem, stream) : launch_tt<1, 0, 0>(p, fp.smem, stream);
+  else if (T <= 2)
+    e = xing4 ? launch_tt<2, 7, 64>(p, fp.smem, stream) : launch_tt<2, 0, 0>(p, fp.smem, stream);
+  else if (T <= 4)
+    e = xing4 ? launch_tt<4, 7, 64>(p, fp.smem, stream) : launch_tt<4, 0, 0>(p, fp.smem, stream);
+  else
+    e = xing4 ? launch_tt<8, 7, 64>(p, fp.smem, stream) : launch_tt<8, 0, 0>(p, fp.smem, stream);
+  count_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace moe

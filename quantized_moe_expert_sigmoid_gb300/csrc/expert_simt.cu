@@ -23,9 +23,10 @@ namespace {
 
 // IQ4_NL 16-entry table (HelloSun/xing4_0-29b-IQ4_NL_EPQ model card:
 // "16-entry nonlinear table + single fp16 scale"; values as given with the
-// synthetic workload definition).
-__constant__ float c_codebook[16] = {-127.f, -104.f, -83.f, -65.f, -49.f, -35.f, -22.f, -10.f,
-                                     1.f,    13.f,   25.f,  38.f,  53.f,  69.f,  89.f,  113.f};
+// synthetic workload definition), in the layer's label order: label j < 8
+// is table entry 2j, label j + 8 is entry 2j + 1.
+__constant__ float c_codebook[16] = {-127.f, -83.f, -49.f, -22.f, 1.f,  25.f, 53.f, 89.f,
+                                     -104.f, -65.f, -35.f, -10.f, 13.f, 38.f, 69.f, 113.f};
 
 __device__ __forceinline__ void load_x8(const float *p, float v[8]) {
   const float4 a = *reinterpret_cast<const float4 *>(p);

@@ -31,6 +31,9 @@ constexpr int kSBW = 256;       // weights per superblock
 constexpr int kSBBytes = 144;   // bytes per superblock
 constexpr int kGroupRows = 64;  // gate/up interleave group
 
+// Largest batch the single-launch decode kernel handles.
+constexpr int kFusedMaxTokens = 8;
+
 // Sticky device error bits (Layer::err).
 constexpr unsigned kErrBadId = 1u;
 constexpr unsigned kErrTimeout = 2u;
@@ -61,6 +64,7 @@ struct Layer {
   float *h32 = nullptr;      // [max_routes][Fp] SwiGLU output (fp32)
   float *out_acc = nullptr;  // [max_tokens][H] fp32 accumulator
   unsigned *err = nullptr;   // sticky device error word
+  unsigned *sync = nullptr;  // [4] arrival counters of the single-launch decode kernel
 };
 
 // Launch counter behind moe_launch_count(); every launcher adds its kernels.
@@ -97,6 +101,16 @@ cudaError_t launch_upgate_simt(const Layer &L, const void *x, moe_dtype xdt, int
 cudaError_t launch_down_simt(const Layer &L, int T, cudaStream_t stream);
 cudaError_t launch_finalize(const Layer &L, int T, void *out, moe_dtype odt,
                             cudaStream_t stream);
+
+// decode_fused.cu: the whole layer in one launch for T <= kFusedMaxTokens.
+// ids_in == nullptr: route inside (router_w, bias used; ids_out/w_out
+// written); else the given routes are used.
+size_t smem_limit_fused();
+bool fused_decode_supported(const Layer &L, int T);
+cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, int T,
+                                const float *wr, const float *bias, int64_t bstride,
+                                const int32_t *ids_in, const float *w_in, int32_t *ids_out,
+                                float *w_out, void *out, moe_dtype odt, cudaStream_t stream);
 
 // norm.cu
 cudaError_t launch_residual_rmsnorm(float *resid, const void *delta, moe_dtype ddt,

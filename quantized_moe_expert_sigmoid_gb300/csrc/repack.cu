@@ -3,7 +3,9 @@
 // Source block (HelloSun/xing4_0-29b-IQ4_NL_EPQ model card, "對純 NumPy"):
 // an fp16 scale then 16 index bytes; weight j (0..15) is the low nibble of
 // byte j and weight j+16 its high nibble.  Destination: the 8 scales of a
-// superblock first, then each block's indices with weight m in nibble m.
+// superblock first, then each block's 4-bit labels with weight m in nibble m.
+// A label is the table index relabelled as (i >> 1) + 8 * (i & 1), which puts
+// same-sign table entries at labels j and j + 8 (see device_utils.cuh).
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -35,8 +37,9 @@ __global__ void repack_kernel(const uint8_t *__restrict__ src, int rows, int K,
       uint8_t w[32];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        w[i] = blk[2 + i] & 15;
-        w[i + 16] = blk[2 + i] >> 4;
+        const int lo = blk[2 + i] & 15, hi = blk[2 + i] >> 4;
+        w[i] = (uint8_t)((lo >> 1) + 8 * (lo & 1));
+        w[i + 16] = (uint8_t)((hi >> 1) + 8 * (hi & 1));
       }
 #pragma unroll
       for (int i = 0; i < 16; ++i) out[16 + 16 * j + i] = (uint8_t)(w[2 * i] | (w[2 * i + 1] << 4));

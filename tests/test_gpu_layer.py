@@ -214,3 +214,55 @@ def test_binding_refuses_strided_and_mistyped_tensors():
         L.forward(x, ids.long(), torch.from_numpy(c.w.astype(np.float32)).cuda())
     with pytest.raises(ValueError):
         L.route(x.t().contiguous().t(), wr)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 8])
+def test_single_launch_decode_matches_oracle(T):
+    """Batches of up to 8 tokens run the whole layer in one launch."""
+    import quantized_moe_expert_sigmoid_gb300 as moe
+    wl = synth.WORKLOADS["decode1"]
+    ew = parity.weights(0, 0, wl.E, wl.H, wl.F, 1)
+    c = cases.make_case(wl, T=T, ew=ew, seed=0)
+    L = _layer_for("decode1")
+    x, wr, _ = _dev_inputs(c)
+    before = moe.moe_launch_count()
+    out, ids, w = L.forward_routed(x, wr, out_dtype=torch.float32)
+    assert moe.moe_launch_count() - before == 1
+    L.check()
+    np.testing.assert_array_equal(ids.cpu().numpy(), c.ids)
+    np.testing.assert_allclose(w.cpu().numpy(), c.w, rtol=0, atol=2e-6)
+    ref = oracle.moe_forward(c.x64, c.ids, c.w, c.ew)
+    parity.assert_close_fp32(out.cpu().numpy(), ref, f"T={T}")
+    out2 = L.forward(x, ids, w, out_dtype=torch.float32)
+    L.check()
+    parity.assert_close_fp32(out2.cpu().numpy(), ref, f"T={T} given routes")
+
+
+def test_graph_replay_matches_eager():
+    """Layer calls captured in a CUDA graph (with programmatic dependent
+    launch between them) give the eager results."""
+    import quantized_moe_expert_sigmoid_gb300 as moe
+    c = _case("decode1")
+    L = _layer_for("decode1")
+    x, wr, _ = _dev_inputs(c)
+    xs = [x.clone() for _ in range(4)]
+    for i, xi in enumerate(xs):
+        xi.mul_(1.0 + 0.25 * i)
+    ids = [torch.empty((1, 4), dtype=torch.int32, device="cuda") for _ in xs]
+    ws = [torch.empty((1, 4), dtype=torch.float32, device="cuda") for _ in xs]
+    outs = [torch.empty((1, 3584), dtype=torch.bfloat16, device="cuda") for _ in xs]
+    eager = []
+    for i, xi in enumerate(xs):
+        o, _, _ = L.forward_routed(xi, wr)
+        eager.append(o.float().cpu())
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i, xi in enumerate(xs):
+            moe.moe_layer_forward_routed(L.handle, xi, wr, ids[i], ws[i], outs[i])
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    L.check()
+    for i in range(len(xs)):
+        assert torch.allclose(outs[i].float().cpu(), eager[i], rtol=0, atol=2e-2 * eager[i].abs().max().item())
