@@ -153,6 +153,28 @@ moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype 
 moe_status moe_residual_rmsnorm(float *resid, const void *delta, moe_dtype delta_dtype,
                                 void *u, int32_t T, int32_t H, float eps, void *stream);
 
+/* Router for callers that cannot allocate device memory.  The paper has no
+ * counterpart: this entry point exists for callers that may not call
+ * cudaMalloc themselves or let a library do it -- code inside a host
+ * framework that owns every device allocation, a stream-ordered pool that
+ * must not grow, or a serving step that may not allocate once it is up.
+ * It computes exactly what moe_route computes (same kernels, same arguments
+ * and layouts, no layer object), but its fp32 logits scratch is a fixed
+ * file-scope device array of 262,144 floats (1 MiB) that every GPU which
+ * loads the library keeps until the process exits.
+ *   T * n_experts > 262,144 returns MOE_ERR_UNSUPPORTED_SHAPE; nothing is
+ *   allocated or freed.  The first call on a device looks up the array's
+ *   device address (cudaGetSymbolAddress) and caches it, so make that first
+ *   call before any stream capture.  Every call shares the one array: calls
+ *   whose kernels overlap on the GPU (for example on two streams) race on
+ *   it.  The scratch is fully written before it is read, so nothing needs
+ *   clearing between calls. */
+moe_status moe_route_noalloc(const void *x, moe_dtype x_dtype, int32_t T, int32_t hidden,
+                             int32_t n_experts, int32_t top_k, float routed_scaling,
+                             const float *router_w, const float *logit_bias,
+                             int64_t bias_row_stride, int32_t *ids, float *weights,
+                             void *stream);
+
 /* Synchronise the device and report (then clear) the layer's sticky device
  * error: MOE_OK, MOE_ERR_BAD_EXPERT_ID or MOE_ERR_TIMEOUT. */
 moe_status moe_layer_check(moe_layer_t layer);

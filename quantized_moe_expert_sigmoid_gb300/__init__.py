@@ -25,7 +25,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 
 EXPORTS = ["moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
            "moe_layer_forward_routed", "moe_residual_rmsnorm", "moe_layer_check",
-           "moe_layer_weight_bytes", "moe_launch_count", "moe_status_string", "moe_last_error"]
+           "moe_layer_weight_bytes", "moe_launch_count", "moe_status_string", "moe_last_error",
+           "moe_route_noalloc"]
 
 
 class MoeError(RuntimeError):
@@ -74,6 +75,8 @@ def load_library(path: str | None = None):
     lib.moe_layer_check.argtypes = [P]
     lib.moe_layer_weight_bytes.argtypes = [P]
     lib.moe_layer_weight_bytes.restype = I64
+    lib.moe_route_noalloc.argtypes = [P, I32, I32, I32, I32, I32, F, P, P, I64, P, P, P]
+    lib.moe_route_noalloc.restype = I32
     lib.moe_launch_count.argtypes = []
     lib.moe_launch_count.restype = I64
     lib.moe_status_string.argtypes = [I32]
@@ -189,6 +192,29 @@ def moe_layer_forward_routed(layer, x, router_w, ids, weights, out, logit_bias=N
         _ptr(router_w, "router_w", d["f32"]), bias_p, bias_row_stride,
         _ptr(ids, "ids", d["i32"]), _ptr(weights, "weights", d["f32"]), _ptr(out, "out", d["x"]),
         _dtype(out), _stream(stream)))
+
+
+def moe_route_noalloc(x, router_w, ids, weights, top_k, routed_scaling=2.0, logit_bias=None,
+                      bias_row_stride=None, stream=None):
+    """moe_route without a layer and without any device allocation: the
+    logits scratch is a fixed array inside the library (T * n_experts <=
+    262,144).  For callers that may not allocate device memory; the first
+    call on a device should come before any stream capture, and calls that
+    overlap on the GPU share (and race on) the one scratch array."""
+    if bias_row_stride is None:
+        bias_row_stride = 0 if logit_bias is None or logit_bias.dim() == 1 else logit_bias.stride(0)
+    d = _dt()
+    if logit_bias is not None and logit_bias.dim() == 2 and logit_bias.stride(1) == 1 \
+            and bias_row_stride == logit_bias.stride(0):
+        bias_p = ctypes.c_void_p(logit_bias.data_ptr())
+    else:
+        bias_p = _ptr(logit_bias, "logit_bias", d["f32"])
+    T, H = x.shape
+    E = router_w.shape[0]
+    _check(load_library().moe_route_noalloc(
+        _ptr(x, "x", d["x"]), _dtype(x), T, H, E, top_k, float(routed_scaling),
+        _ptr(router_w, "router_w", d["f32"]), bias_p, bias_row_stride,
+        _ptr(ids, "ids", d["i32"]), _ptr(weights, "weights", d["f32"]), _stream(stream)))
 
 
 def moe_residual_rmsnorm(resid, delta, u, eps, stream=None):

@@ -33,6 +33,18 @@ moe_status fail(moe_status s, const char *fmt, ...) {
   return s;
 }
 
+}  // namespace
+
+moe_status moe::report_error(moe_status s, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+namespace {
+
 moe_status cuda_fail(cudaError_t e, const char *where) {
   if (e == cudaErrorMemoryAllocation)
     return fail(MOE_ERR_OUT_OF_MEMORY, "%s: %s", where, cudaGetErrorString(e));

@@ -67,6 +67,10 @@ struct Layer {
   unsigned *sync = nullptr;  // [4] arrival counters of the single-launch decode kernel
 };
 
+// Records the detail string behind moe_last_error() for the calling thread
+// and returns `s` (printf-style).
+moe_status report_error(moe_status s, const char *fmt, ...);
+
 // Launch counter behind moe_launch_count(); every launcher adds its kernels.
 void count_launches(int n);
 

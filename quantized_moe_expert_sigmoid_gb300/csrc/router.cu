@@ -13,6 +13,8 @@
 // selected; w = scale * s / sum(s).
 #include <float.h>
 
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -233,3 +235,90 @@ cudaError_t launch_router_topk(const Layer &L, const float *logits, int T, int32
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Router for callers that cannot allocate device memory.
+//
+// Some callers may not call cudaMalloc at all: code running where the
+// allocator is owned by someone else (a host framework's memory pool, a
+// stream-ordered pool that must not grow), or a step that may not allocate
+// once a service is up.  moe_route_noalloc runs the same two router kernels
+// as moe_route, but the logits scratch lives in the file-scope array below
+// instead of a layer's workspace, and no layer is needed.
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+constexpr int64_t kNoAllocMaxLogits = int64_t(1) << 18;  // T * n_experts <= 262,144 (1 MiB)
+static __device__ __align__(256) float g_noalloc_logits[kNoAllocMaxLogits];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is asked of
+// the runtime once per device (with that device current) and cached.
+cudaError_t noalloc_scratch(float **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_logits);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<float *>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_route_noalloc(const void *x, moe_dtype x_dtype, int32_t T,
+                                        int32_t hidden, int32_t n_experts, int32_t top_k,
+                                        float routed_scaling, const float *router_w,
+                                        const float *logit_bias, int64_t bias_row_stride,
+                                        int32_t *ids, float *weights, void *stream) {
+  using moe::report_error;
+  if (T < 0) return report_error(MOE_ERR_INVALID_ARG, "T = %d is negative", T);
+  if (x_dtype != MOE_DT_BF16 && x_dtype != MOE_DT_FP32)
+    return report_error(MOE_ERR_INVALID_ARG, "x_dtype %d is not MOE_DT_BF16 or MOE_DT_FP32", (int)x_dtype);
+  if (hidden < 32 || hidden > 16384 || hidden % 32)
+    return report_error(MOE_ERR_UNSUPPORTED_SHAPE, "hidden = %d: need a multiple of 32 in [32, 16384]", hidden);
+  if (n_experts < 1 || n_experts > 256)
+    return report_error(MOE_ERR_UNSUPPORTED_SHAPE, "n_experts = %d: need 1..256", n_experts);
+  if (top_k < 1 || top_k > 8 || top_k > n_experts)
+    return report_error(MOE_ERR_UNSUPPORTED_SHAPE, "top_k = %d: need 1..min(n_experts, 8)", top_k);
+  if (!(routed_scaling > 0.f)) return report_error(MOE_ERR_INVALID_ARG, "routed_scaling must be > 0");
+  if ((int64_t)T * n_experts > moe::kNoAllocMaxLogits)
+    return report_error(MOE_ERR_UNSUPPORTED_SHAPE,
+                        "T * n_experts = %lld exceeds the %lld-logit scratch of moe_route_noalloc",
+                        (long long)T * n_experts, (long long)moe::kNoAllocMaxLogits);
+  if (T == 0) return MOE_OK;
+  if (!x || !router_w || !ids || !weights)
+    return report_error(MOE_ERR_INVALID_ARG, "x, router_w, ids and weights must be non-NULL");
+  if (!moe::aligned(x, 16) || !moe::aligned(router_w, 16) || (logit_bias && !moe::aligned(logit_bias, 16)))
+    return report_error(MOE_ERR_MISALIGNED, "x, router_w and logit_bias must be 16-byte aligned");
+  if (!moe::aligned(ids, 4) || !moe::aligned(weights, 4))
+    return report_error(MOE_ERR_MISALIGNED, "ids/weights are not 4-byte aligned");
+  if (logit_bias && bias_row_stride < 0)
+    return report_error(MOE_ERR_INVALID_ARG, "bias_row_stride is negative");
+  float *logits = nullptr;
+  cudaError_t e = moe::noalloc_scratch(&logits);
+  if (e != cudaSuccess)
+    return report_error(MOE_ERR_CUDA, "moe_route_noalloc scratch address: %s", cudaGetErrorString(e));
+  moe::Layer L;  // shape fields only; the router kernels read nothing else
+  L.H = hidden;
+  L.E = n_experts;
+  L.k = top_k;
+  L.scale = routed_scaling;
+  cudaStream_t st = (cudaStream_t)stream;
+  e = moe::launch_router_logits(L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, logits, st);
+  if (e == cudaSuccess) e = moe::launch_router_topk(L, logits, T, ids, weights, st);
+  if (e != cudaSuccess) return report_error(MOE_ERR_CUDA, "moe_route_noalloc: %s", cudaGetErrorString(e));
+  return MOE_OK;
+}
