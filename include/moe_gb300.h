@@ -58,7 +58,9 @@ typedef enum {
   MOE_ERR_CUDA = 5,              /* a CUDA call failed; see moe_last_error  */
   MOE_ERR_TIMEOUT = 6,           /* a bounded device wait gave up           */
   MOE_ERR_BAD_EXPERT_ID = 7,     /* an id outside [0, E) reached forward    */
-  MOE_ERR_TOO_MANY_TOKENS = 8    /* T > max_tokens given at create          */
+  MOE_ERR_TOO_MANY_TOKENS = 8,   /* T > max_tokens given at create          */
+  MOE_ERR_OVERFLOW = 9           /* an activation left fp16 range (batched  *
+                                  * tensor-core path); outputs are invalid  */
 } moe_status;
 
 typedef enum { MOE_DT_BF16 = 0, MOE_DT_FP32 = 1 } moe_dtype;
@@ -176,7 +178,9 @@ moe_status moe_route_noalloc(const void *x, moe_dtype x_dtype, int32_t T, int32_
                              void *stream);
 
 /* Synchronise the device and report (then clear) the layer's sticky device
- * error: MOE_OK, MOE_ERR_BAD_EXPERT_ID or MOE_ERR_TIMEOUT. */
+ * error: MOE_OK, MOE_ERR_BAD_EXPERT_ID, MOE_ERR_TIMEOUT or MOE_ERR_OVERFLOW
+ * (batches of more than 8 tokens run on fp16 tensor-core operands; an input
+ * or SwiGLU value beyond fp16 range is reported, never silently clipped). */
 moe_status moe_layer_check(moe_layer_t layer);
 
 /* Bytes of IQ4_NL weights held for the layer (routed + shared). */

@@ -21,7 +21,8 @@ MOE_DT_FP32 = 1
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_OUT_OF_MEMORY", 5: "MOE_ERR_CUDA",
-          6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_BAD_EXPERT_ID", 8: "MOE_ERR_TOO_MANY_TOKENS"}
+          6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_BAD_EXPERT_ID", 8: "MOE_ERR_TOO_MANY_TOKENS",
+          9: "MOE_ERR_OVERFLOW"}
 
 EXPORTS = ["moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
            "moe_layer_forward_routed", "moe_residual_rmsnorm", "moe_layer_check",

@@ -71,7 +71,8 @@ bool is_device_ptr(const void *p) {
 void free_layer(Layer *L) {
   if (!L) return;
   void *ptrs[] = {L->gu, L->dn, L->logits, L->offsets, L->active, L->route_token,
-                  L->route_weight, L->h32, L->out_acc, L->err, L->sync};
+                  L->route_weight, L->h32, L->out_acc, L->err, L->sync, L->x16, L->h16,
+                  L->tiles_ug, L->tiles_dn, L->tile_counts};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   delete L;
@@ -124,8 +125,7 @@ moe_status forward_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const
   }
   MOE_CUDA(cudaMemsetAsync(L->out_acc, 0, sizeof(float) * (size_t)T * L->H, st), "clear accumulator");
   MOE_CUDA(moe::launch_route_plan(*L, ids, w, T, st), "route plan");
-  MOE_CUDA(moe::launch_upgate_simt(*L, x, xdt, T, st), "up/gate");
-  MOE_CUDA(moe::launch_down_simt(*L, T, st), "down");
+  MOE_CUDA(moe::launch_prefill_tc(*L, x, xdt, T, st), "tensor-core expert GEMMs");
   MOE_CUDA(moe::launch_finalize(*L, T, out, odt, st), "finalize");
   return MOE_OK;
 }
@@ -145,6 +145,7 @@ const char *moe_status_string(moe_status s) {
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
     case MOE_ERR_BAD_EXPERT_ID: return "MOE_ERR_BAD_EXPERT_ID";
     case MOE_ERR_TOO_MANY_TOKENS: return "MOE_ERR_TOO_MANY_TOKENS";
+    case MOE_ERR_OVERFLOW: return "MOE_ERR_OVERFLOW";
   }
   return "MOE_ERR_UNKNOWN";
 }
@@ -208,6 +209,13 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   ALLOC(L->out_acc, sizeof(float) * (int64_t)sh->max_tokens * H);
   ALLOC(L->err, sizeof(unsigned));
   ALLOC(L->sync, 4 * sizeof(unsigned));
+  // batched tensor-core path (also taken by small batches whose shape the
+  // single-launch decode kernel does not cover)
+  ALLOC(L->x16, sizeof(__half) * (int64_t)L->max_routes * L->Hp);
+  ALLOC(L->h16, sizeof(__half) * (int64_t)L->max_routes * L->Fp);
+  ALLOC(L->tiles_ug, sizeof(moe::TcTile) * (int64_t)moe::tc_max_tiles(*L, true));
+  ALLOC(L->tiles_dn, sizeof(moe::TcTile) * (int64_t)moe::tc_max_tiles(*L, false));
+  ALLOC(L->tile_counts, 2 * sizeof(int));
 #undef ALLOC
 
   cudaError_t e = cudaSuccess;
@@ -229,6 +237,7 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
       e = moe::launch_repack(up, F, H, gu, L->gu_row_bytes, 2 * moe::kGroupRows, moe::kGroupRows, st);
     if (e == cudaSuccess) e = moe::launch_repack(down, H, F, dn, L->dn_row_bytes, 0, 0, st);
   }
+  if (e == cudaSuccess) e = moe::tc_prepare(*L);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {
     free_layer(L);
@@ -310,6 +319,7 @@ moe_status moe_layer_check(moe_layer_t layer) {
   MOE_CUDA(cudaMemcpy(&err, L->err, sizeof(unsigned), cudaMemcpyDeviceToHost), "read error word");
   MOE_CUDA(cudaMemset(L->err, 0, sizeof(unsigned)), "clear error word");
   if (err & moe::kErrTimeout) return fail(MOE_ERR_TIMEOUT, "a bounded device wait gave up");
+  if (err & moe::kErrOverflow) return fail(MOE_ERR_OVERFLOW, "an activation left fp16 range on the tensor-core path");
   if (err & moe::kErrBadId) return fail(MOE_ERR_BAD_EXPERT_ID, "an expert id outside [0, E) reached moe_forward");
   return MOE_OK;
 }

@@ -56,6 +56,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   return false;
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of `bar` for at most about `budget_ns` of wall
+// time (the global timer is read every 64 polls); false on timeout.
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t *bar, uint32_t parity, uint64_t budget_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > budget_ns) return false;
+  }
+}
+
 // 1D bulk copy global -> shared, completing on `bar` (16-byte aligned
 // addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,

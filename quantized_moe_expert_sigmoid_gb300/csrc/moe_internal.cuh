@@ -17,6 +17,7 @@
 // The shared expert is stored as expert index E.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -37,6 +38,13 @@ constexpr int kFusedMaxTokens = 8;
 // Sticky device error bits (Layer::err).
 constexpr unsigned kErrBadId = 1u;
 constexpr unsigned kErrTimeout = 2u;
+constexpr unsigned kErrOverflow = 4u;  // a value left fp16 range on the tensor-core path
+
+// One tile of the batched tensor-core path: expert id, 128-row weight tile,
+// first route row (in route order) and number of routes (<= 256).
+struct TcTile {
+  int expert, mtile, row0, count;
+};
 
 struct Layer {
   // shape
@@ -65,6 +73,13 @@ struct Layer {
   float *out_acc = nullptr;  // [max_tokens][H] fp32 accumulator
   unsigned *err = nullptr;   // sticky device error word
   unsigned *sync = nullptr;  // [4] arrival counters of the single-launch decode kernel
+
+  // batched tensor-core path (T > kFusedMaxTokens)
+  __half *x16 = nullptr;     // [max_routes][Hp] x rows in route order, fp16
+  __half *h16 = nullptr;     // [max_routes][Fp] SwiGLU outputs, fp16
+  TcTile *tiles_ug = nullptr, *tiles_dn = nullptr;
+  int *tile_counts = nullptr;  // [2]
+  CUtensorMap map_gu_raw, map_dn_raw, map_x16, map_h16;
 };
 
 // Records the detail string behind moe_last_error() for the calling thread
@@ -115,6 +130,11 @@ cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, in
                                 const float *wr, const float *bias, int64_t bstride,
                                 const int32_t *ids_in, const float *w_in, int32_t *ids_out,
                                 float *w_out, void *out, moe_dtype odt, cudaStream_t stream);
+
+// prefill_tc.cu: grouped GEMMs on tcgen05 for T > kFusedMaxTokens.
+int tc_max_tiles(const Layer &L, bool up_gate);
+cudaError_t tc_prepare(Layer &L);  // tensor maps + kernel attributes (after workspace allocation)
+cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int T, cudaStream_t stream);
 
 // norm.cu
 cudaError_t launch_residual_rmsnorm(float *resid, const void *delta, moe_dtype ddt,
