@@ -549,19 +549,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);  // this warp is done with the stage
-      if (fl < it.count) {
-        float v[TT];
+      // The pair meets at every item, also one that has no output f0 + fl:
+      // up_part is double-buffered by item parity, so the up warp may only
+      // write item i + 2's value after the gate warp has read item i's,
+      // which the barrier of item i + 1 guarantees.
+      float v[TT];
 #pragma unroll
-        for (int r = 0; r < TT; ++r) v[r] = r < nr ? warp_sum(acc[r]) : 0.f;
-        if (is_up && lane == 0)
-          for (int r = 0; r < nr; ++r) up_part[i & 1][fl][r] = v[r];
-        named_sync(kBarPair0 + fl, 64);
-        if (!is_up && lane == 0)
-          for (int r = 0; r < nr; ++r) {
-            const float g = v[r], u = up_part[i & 1][fl][r];
-            L.h32[(int64_t)(rs + r) * Fp + it.f0 + fl] = g / (1.0f + expf(-g)) * u;
-          }
-      }
+      for (int r = 0; r < TT; ++r) v[r] = r < nr ? warp_sum(acc[r]) : 0.f;
+      if (fl < it.count && is_up && lane == 0)
+        for (int r = 0; r < nr; ++r) up_part[i & 1][fl][r] = v[r];
+      named_sync(kBarPair0 + fl, 64);
+      if (fl < it.count && !is_up && lane == 0)
+        for (int r = 0; r < nr; ++r) {
+          const float g = v[r], u = up_part[i & 1][fl][r];
+          L.h32[(int64_t)(rs + r) * Fp + it.f0 + fl] = g / (1.0f + expf(-g)) * u;
+        }
     };
 
     int i = 0;

@@ -40,8 +40,9 @@ constexpr unsigned kErrBadId = 1u;
 constexpr unsigned kErrTimeout = 2u;
 constexpr unsigned kErrOverflow = 4u;  // a value left fp16 range on the tensor-core path
 
-// One tile of the batched tensor-core path: expert id, 128-row weight tile,
-// first route row (in route order) and number of routes (<= 256).
+// One tile of the batched tensor-core path: expert id, weight tile (128
+// up/gate outputs or 256 down rows), first route row (in route order) and
+// number of routes (<= 256).
 struct TcTile {
   int expert, mtile, row0, count;
 };
@@ -79,7 +80,8 @@ struct Layer {
   __half *h16 = nullptr;     // [max_routes][Fp] SwiGLU outputs, fp16
   TcTile *tiles_ug = nullptr, *tiles_dn = nullptr;
   int *tile_counts = nullptr;  // [2]
-  CUtensorMap map_gu_raw, map_dn_raw, map_x16, map_h16;
+  CUtensorMap map_x16, map_h16;        // activation tiles of the tensor-core path
+  CUtensorMap map_gu_lab, map_dn_lab;  // weight labels of one k-step
 };
 
 // Records the detail string behind moe_last_error() for the calling thread

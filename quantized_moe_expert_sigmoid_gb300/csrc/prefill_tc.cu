@@ -5,26 +5,32 @@
 // table of PocketLLM's "Xing4.0-29B-A4B: the design record", section 4,
 // re-built for tcgen05:
 //   gather     x rows of every route -> fp16 rows in route order (x16)
-//   up/gate    per tile (expert, 128 outputs, <= 256 routes):
-//              G = Wg x16^T and U = Wu x16^T in two TMEM accumulators
-//              (M = 128, N = routes, K = hidden), h = silu(G) * U -> fp16
-//   down       per tile (expert, 128 hidden rows, <= 256 routes):
-//              Y = Wd h^T; out_acc[token][row] += route weight * Y (fp32)
+//   up/gate    per tile (expert, 128 outputs, <= 256 routes): the gate and
+//              the up rows of the same outputs are two M = 128 MMAs on one
+//              activation tile, G = Wg x16^T and U = Wu x16^T in two TMEM
+//              accumulators; h = silu(G) * U -> fp16
+//   down       per tile (expert, 256 hidden rows, <= 256 routes): two
+//              M = 128 MMAs on one h tile; out_acc[token][row] +=
+//              route weight * Y (fp32)
 //   finalize   out = round(out_acc)
 // Operands are fp16 (kind::f16, fp32 accumulate): the IQ4_NL codes are
 // integers |c| <= 127, exact in fp16, and the per-block scale is applied when
 // a tile is dequantised (one rounding of d * code); bf16 weights and h would
 // cost ~3e-3 mean relative error on this layer, fp16 ~4e-4.
 //
-// CTA (persistent, one per SM, 288 threads):
-//   warp 0     producer: 2D TMA copies of raw IQ4_NL superblock columns
-//              (144-byte units, no swizzle) and of the fp16 activation tile
-//              for every 64-wide k-step (128-byte swizzle, K-major)
-//   warps 1-8  consumers: dequantise the raw rows into fp16 A tiles in the
-//              same 128-byte-swizzled K-major layout; after a named barrier
-//              one thread issues the tcgen05.mma of the k-step and commits
-//              them to the stage's "empty" mbarrier; after a tile, the same
-//              warps read TMEM (tcgen05.ld 32x32b) for the epilogue.
+// CTA (persistent, one per SM, 19 warps):
+//   warp 0      activation producer: 2D TMA copies of the fp16 activation
+//               tile of every 64-wide k-step (128-byte swizzle, K-major)
+//   warp 1      owns TMEM; one thread issues the tcgen05.mma of each k-step
+//               once its A and B stages are full and commits them to the
+//               stages' "empty" mbarriers
+//   warp 2      weight producer: 2D TMA copies of the 4-bit labels of every
+//               k-step (32 bytes of each of the tile's 256 weight rows)
+//   warps 3-18  dequantisers (two threads per weight row, 32 weights of a
+//               k-step each; the fp16 block scales come from global memory
+//               one superblock ahead): fp16 d * code into the 128-byte-
+//               swizzled K-major A stages; after a tile the same warps read
+//               TMEM (tcgen05.ld 32x32b) for the epilogue
 // Every wait is bounded; a timeout sets the layer's sticky error word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -37,17 +43,24 @@
 namespace moe {
 namespace {
 
-constexpr int kNT = 256;   // routes per tile (MMA N upper bound)
-constexpr int kTM = 128;   // weight rows per MMA (M)
-constexpr int kKS = 64;    // K per k-step: one 128-byte swizzle row of fp16
-constexpr int kConsWarps = 8;
-constexpr int kCons = kConsWarps * 32;
-constexpr int kThreadsTC = kCons + 32;
-constexpr int kOpStages = 2;
-constexpr int kRawStages = 2;
-constexpr int kATile = kTM * kKS * 2;  // 16 KB
-constexpr int kBTile = kNT * kKS * 2;  // 32 KB
+constexpr int kNT = 256;            // routes per tile (MMA N upper bound)
+constexpr int kTM = 128;            // rows per MMA (M)
+constexpr int kRowsTile = 2 * kTM;  // weight rows per tile: two MMAs share each B tile
+constexpr int kKS = 64;             // K per k-step: one 128-byte swizzle row of fp16
+constexpr int kKSteps = kSBW / kKS; // k-steps per superblock
+constexpr int kDqWarps = 16;
+constexpr int kDq = kDqWarps * 32;  // two dequantising threads per weight row
+constexpr int kDqWarp0 = 3;         // warps 0..2: activation producer, MMA, weight producer
+constexpr int kThreadsTC = kDq + 32 * kDqWarp0;
+constexpr int kAStages = 3;
+constexpr int kBStages = 3;
+constexpr int kLabStages = 4;
+constexpr int kATile = kTM * kKS * 2;        // 16 KB
+constexpr int kAStage = 2 * kATile;          // 32 KB
+constexpr int kBTile = kNT * kKS * 2;        // 32 KB
+constexpr int kLabStage = kRowsTile * 32;    // labels of one k-step: 32 bytes per row
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait before the CTA gives up
+static_assert(kDq == 2 * kRowsTile, "two dequantising threads per weight row");
 
 // labels -> biased bytes (code + 128) for the fp16 conversion: the int8
 // decode of device_utils.cuh with every code's sign bit flipped afterwards
@@ -105,17 +118,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
-      " [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -126,14 +128,15 @@ __device__ __forceinline__ void tc_fence_after() {
 struct TcParams {
   const TcTile *tiles;
   const int *n_tiles;
+  const uint8_t *w;          // superblock rows of this matrix kind, all experts
+  int64_t row_bytes;         // bytes per weight row
+  int64_t rows_per_expert;   // 2 * Fp (up/gate) or Hp (down)
   const int *route_token;
   const float *route_weight;
   __half *h16;       // up/gate output [routes][Fp]
   float *out_acc;    // down output accumulator [T][H]
   unsigned *err;
   int H, Hp, Fp;
-  int64_t gu_rows_per_expert;  // 2 * Fp
-  int64_t dn_rows_per_expert;  // Hp
 };
 
 // Bounded wait shared by all roles: once any wait of the CTA has run out
@@ -144,43 +147,68 @@ __device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity, vo
   if (!mbar_wait_ns(bar, parity, kWaitNs)) *abort = 1;
 }
 
-// UG = true: up/gate (two A tiles per k-step: gate and up rows of the same
-// 128 outputs); UG = false: down (one A tile of 128 hidden rows).
+// Weight row (within its expert) that tile row r (0..255) of m-tile m
+// reads.  Up/gate: rows 0..127 are the gate rows, 128..255 the up rows, of
+// outputs 128m..128m+127; the matrix interleaves gate and up in groups of
+// 64 rows (group g: gate of outputs 64g.., then up of the same outputs).
+template <bool UG>
+__device__ __forceinline__ int tile_row(int m, int r) {
+  if (UG) {
+    const int a = r >> 7, rr = r & (kTM - 1);
+    return 4 * kGroupRows * m + a * kGroupRows + (rr < kGroupRows ? rr : rr + kGroupRows);
+  }
+  return kRowsTile * m + r;
+}
+
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
+      " [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// UG = true: up/gate + SwiGLU epilogue; UG = false: down + weighted scatter.
 template <bool UG>
 __global__ void __launch_bounds__(kThreadsTC, 1)
-    grouped_gemm_tc(const TcParams p, const __grid_constant__ CUtensorMap raw_map,
-                    const __grid_constant__ CUtensorMap b_map) {
-  constexpr int NA = UG ? 2 : 1;
-  constexpr int kRawRows = NA * kTM;
-  constexpr int kRawBytes = kRawRows * kSBBytes;
-  constexpr int kOpBytes = NA * kATile + kBTile;
-  constexpr int kTmemCols = UG ? 512 : 256;
-  constexpr int kKSteps = kSBW / kKS;
+    grouped_gemm_tc(const TcParams p, const __grid_constant__ CUtensorMap b_map,
+                    const __grid_constant__ CUtensorMap lab_map) {
+  constexpr int kTmemCols = 2 * kNT;
   extern __shared__ uint8_t smem_dyn[];
-  __shared__ uint64_t op_full[kOpStages], op_empty[kOpStages], raw_full[kRawStages],
-      raw_empty[kRawStages], acc_bar, fin_bar;
+  __shared__ uint64_t a_full[kAStages], a_empty[kAStages], b_full[kBStages], b_empty[kBStages],
+      lab_full[kLabStages], lab_empty[kLabStages], acc_full, acc_empty, fin_bar;
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
   volatile int *abort = &abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nsb = (UG ? p.Hp : p.Fp) / kSBW;  // superblock columns along K
+  const int nks = nsb * kKSteps;
   const int ntiles = *p.n_tiles;
   // 128-byte swizzled tiles need 1024-byte aligned bases (the launch adds
   // 1 KB of slack for this)
-  uint8_t *op_base = smem_dyn + ((1024u - (smem_addr(smem_dyn) & 1023u)) & 1023u);
-  uint8_t *raw_base = op_base + kOpStages * kOpBytes;
+  uint8_t *a_base = smem_dyn + ((1024u - (smem_addr(smem_dyn) & 1023u)) & 1023u);
+  uint8_t *b_base = a_base + kAStages * kAStage;
+  uint8_t *lab_base = b_base + kBStages * kBTile;
 
   if (tid == 0) {
-    for (int s = 0; s < kOpStages; ++s) {
-      mbar_init(&op_full[s], 1);
-      mbar_init(&op_empty[s], 1);
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&a_full[s], kDqWarps);
+      mbar_init(&a_empty[s], 1);
     }
-    for (int r = 0; r < kRawStages; ++r) {
-      mbar_init(&raw_full[r], 1);
-      mbar_init(&raw_empty[r], kConsWarps);
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
     }
-    mbar_init(&acc_bar, 1);
+    for (int s = 0; s < kLabStages; ++s) {
+      mbar_init(&lab_full[s], 1);
+      mbar_init(&lab_empty[s], kDqWarps);
+    }
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, kDqWarps);
     mbar_init(&fin_bar, 1);
     fence_mbar_init();
     abort_flag = 0;
@@ -197,180 +225,193 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_holder;
 
-  if (warp == 0) {
-    // ============================ producer ============================
+  if (warp == 0 || warp == 2) {
+    // ===================== producers (activations / labels) =====================
     if (lane == 0) {
-      uint32_t q = 0, v = 0;
+      const bool act = warp == 0;
+      const int nst = act ? kBStages : kLabStages;
+      uint64_t *full = act ? b_full : lab_full;
+      uint64_t *empty = act ? b_empty : lab_empty;
+      uint32_t q = 0;
       for (int ti = blockIdx.x; ti < ntiles && !*abort; ti += gridDim.x) {
         const TcTile t = p.tiles[ti];
-        for (int sbc = 0; sbc < nsb && !*abort; ++sbc, ++v) {
-          const int r = v % kRawStages;
-          if (v >= kRawStages) wait_or_abort(&raw_empty[r], ((v / kRawStages) - 1) & 1u, abort);
+        const int wrow0 = (int)(t.expert * p.rows_per_expert) + t.mtile * kRowsTile;
+        for (int ks = 0; ks < nks; ++ks, ++q) {
+          const int s = q % nst;
+          if (q >= (uint32_t)nst) wait_or_abort(&empty[s], ((q / nst) - 1) & 1u, abort);
           if (*abort) break;
-          uint8_t *raw = raw_base + r * kRawBytes;
-          mbar_arrive_expect_tx(&raw_full[r], kRawBytes);
-          if (UG) {  // gate rows of groups 2m, 2m+1, then their up rows
-            const int row0 = (int)(t.expert * p.gu_rows_per_expert) + t.mtile * (4 * kGroupRows);
-            tma_load_2d(raw, &raw_map, sbc * kSBBytes, row0, &raw_full[r]);
-            tma_load_2d(raw + 64 * kSBBytes, &raw_map, sbc * kSBBytes, row0 + 2 * kGroupRows,
-                        &raw_full[r]);
-            tma_load_2d(raw + 128 * kSBBytes, &raw_map, sbc * kSBBytes, row0 + kGroupRows,
-                        &raw_full[r]);
-            tma_load_2d(raw + 192 * kSBBytes, &raw_map, sbc * kSBBytes, row0 + 3 * kGroupRows,
-                        &raw_full[r]);
+          if (act) {
+            mbar_arrive_expect_tx(&full[s], kBTile);
+            tma_load_2d(b_base + s * kBTile, &b_map, ks * kKS, t.row0, &full[s]);
           } else {
-            const int row0 = (int)(t.expert * p.dn_rows_per_expert) + t.mtile * kTM;
-            tma_load_2d(raw, &raw_map, sbc * kSBBytes, row0, &raw_full[r]);
-          }
-          for (int kk = 0; kk < kKSteps; ++kk, ++q) {
-            const int s = q % kOpStages;
-            if (q >= kOpStages) wait_or_abort(&op_empty[s], ((q / kOpStages) - 1) & 1u, abort);
-            if (*abort) break;
-            uint8_t *bdst = op_base + s * kOpBytes + NA * kATile;
-            mbar_arrive_expect_tx(&op_full[s], kBTile);
-            tma_load_2d(bdst, &b_map, sbc * kSBW + kk * kKS, t.row0, &op_full[s]);
+            uint8_t *dst = lab_base + s * kLabStage;
+            const int xo = (ks >> 2) * kSBBytes + 16 + 32 * (ks & 3);  // blocks 2kk, 2kk+1
+            mbar_arrive_expect_tx(&full[s], kLabStage);
+            if (UG) {  // gate rows of groups 2m, 2m+1, then their up rows (tile_row order)
+              tma_load_2d(dst, &lab_map, xo, wrow0, &full[s]);
+              tma_load_2d(dst + 64 * 32, &lab_map, xo, wrow0 + 2 * kGroupRows, &full[s]);
+              tma_load_2d(dst + 128 * 32, &lab_map, xo, wrow0 + kGroupRows, &full[s]);
+              tma_load_2d(dst + 192 * 32, &lab_map, xo, wrow0 + 3 * kGroupRows, &full[s]);
+            } else {
+              tma_load_2d(dst, &lab_map, xo, wrow0, &full[s]);
+            }
           }
         }
       }
       // no copy may still be landing in shared memory when the CTA exits:
       // wait for the last phase issued on every full barrier (the normal
       // path has consumed them all already, so these return at once)
-      for (int r = 0; r < kRawStages; ++r) {
-        const uint32_t uses = v / kRawStages + ((uint32_t)r < v % kRawStages ? 1u : 0u);
-        if (uses > 0) mbar_wait_ns(&raw_full[r], (uses - 1) & 1u, kWaitNs);
-      }
-      for (int s = 0; s < kOpStages; ++s) {
-        const uint32_t uses = q / kOpStages + ((uint32_t)s < q % kOpStages ? 1u : 0u);
-        if (uses > 0) mbar_wait_ns(&op_full[s], (uses - 1) & 1u, kWaitNs);
+      for (int s = 0; s < nst; ++s) {
+        const uint32_t uses = q / nst + ((uint32_t)s < q % nst ? 1u : 0u);
+        if (uses > 0) mbar_wait_ns(&full[s], (uses - 1) & 1u, kWaitNs);
       }
     }
-  } else {
-    // ============================ consumers ============================
-    // Every consumer thread runs the same trip counts whatever happens, so
-    // the named barrier below always completes; an abort only skips waits
-    // and MMA issue.
-    const int ct = tid - 32;
-    uint32_t q = 0, v = 0, tcount = 0;
-    for (int ti = blockIdx.x; ti < ntiles; ti += gridDim.x) {
-      const TcTile t = p.tiles[ti];
-      const int n_mma = min(kNT, (t.count + 15) & ~15);
-      const uint32_t idesc = (1u << 4) | ((uint32_t)(n_mma >> 3) << 17) | ((uint32_t)(kTM >> 4) << 24);
-      for (int sbc = 0; sbc < nsb; ++sbc, ++v) {
-        const int r = v % kRawStages;
-        wait_or_abort(&raw_full[r], (v / kRawStages) & 1u, abort);
-        const uint8_t *raw = raw_base + r * kRawBytes;
-        for (int kk = 0; kk < kKSteps; ++kk, ++q) {
-          const int s = q % kOpStages;
-          if (q >= kOpStages) wait_or_abort(&op_empty[s], ((q / kOpStages) - 1) & 1u, abort);
-          uint8_t *stage = op_base + s * kOpBytes;
-          // ---- dequantise this k-step's A rows into the swizzled fp16 tile(s)
-          if (UG) {  // thread = one raw row: 0..127 gate, 128..255 up; 64 weights
-            const int rr = ct;
-            const uint8_t *row = raw + rr * kSBBytes;
-            const int tr = rr & (kTM - 1);
-            uint8_t *atile = stage + (rr >> 7) * kATile + tr * 128;
-            const uint32_t sc = *reinterpret_cast<const uint32_t *>(row + 4 * kk);  // 2 fp16 scales
-            const uint4 w0 = *reinterpret_cast<const uint4 *>(row + 16 + 32 * kk);
-            const uint4 w1 = *reinterpret_cast<const uint4 *>(row + 32 + 32 * kk);
-            const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  } else if (warp == 1) {
+    // ============================ MMA issue ============================
+    if (lane == 0) {
+      uint32_t q = 0, tcount = 0;
+      for (int ti = blockIdx.x; ti < ntiles; ti += gridDim.x, ++tcount) {
+        const int count = p.tiles[ti].count;
+        const int n_mma = min(kNT, (count + 15) & ~15);
+        const uint32_t idesc =
+            (1u << 4) | ((uint32_t)(n_mma >> 3) << 17) | ((uint32_t)(kTM >> 4) << 24);
+        if (tcount > 0) wait_or_abort(&acc_empty, (tcount - 1) & 1u, abort);  // TMEM drained
+        tc_fence_after();
+        for (int ks = 0; ks < nks; ++ks, ++q) {
+          const int sa = q % kAStages, sb = q % kBStages;
+          wait_or_abort(&a_full[sa], (q / kAStages) & 1u, abort);
+          wait_or_abort(&b_full[sb], (q / kBStages) & 1u, abort);
+          if (*abort) continue;
+          tc_fence_after();
+          const uint32_t as = smem_addr(a_base + sa * kAStage);
+          const uint32_t bs = smem_addr(b_base + sb * kBTile);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {  // chunk c = weights 8c..8c+7 of the k-step
-              const unsigned short dbits = (unsigned short)(c < 4 ? (sc & 0xFFFF) : (sc >> 16));
-              const __half2 d2 = __half2half2(__ushort_as_half(dbits));
-              uint32_t b0, b1, h0, h1, h2, h3;
-              iq4_decode8_biased(ww[c], b0, b1);
-              codes_to_half(b0, d2, h0, h1);
-              codes_to_half(b1, d2, h2, h3);
-              *reinterpret_cast<uint4 *>(atile + ((c ^ (tr & 7)) << 4)) = make_uint4(h0, h1, h2, h3);
-            }
-          } else {  // two threads per row: block 2kk + half, 32 weights each
-            const int rr = ct >> 1, half = ct & 1;
-            const uint8_t *row = raw + rr * kSBBytes;
-            uint8_t *atile = stage + rr * 128;
-            const unsigned short dbits = *reinterpret_cast<const unsigned short *>(row + 2 * (2 * kk + half));
-            const __half2 d2 = __half2half2(__ushort_as_half(dbits));
-            const uint4 w = *reinterpret_cast<const uint4 *>(row + 16 + 16 * (2 * kk + half));
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          for (int a = 0; a < 2; ++a)
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              const int c = 4 * half + cc;
-              uint32_t b0, b1, h0, h1, h2, h3;
-              iq4_decode8_biased(ww[cc], b0, b1);
-              codes_to_half(b0, d2, h0, h1);
-              codes_to_half(b1, d2, h2, h3);
-              *reinterpret_cast<uint4 *>(atile + ((c ^ (rr & 7)) << 4)) = make_uint4(h0, h1, h2, h3);
-            }
-          }
-          if (kk == kKSteps - 1) {  // this warp is done with the raw stage
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&raw_empty[r]);
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // A tiles -> tensor core
-          named_sync(1, kCons);
-          if (ct == 0) {
-            wait_or_abort(&op_full[s], (q / kOpStages) & 1u, abort);
-            if (!*abort) {
-              tc_fence_after();
-              const uint32_t bsm = smem_addr(stage + NA * kATile);
-#pragma unroll
-              for (int a = 0; a < NA; ++a) {
-                const uint32_t asm_ = smem_addr(stage + a * kATile);
-#pragma unroll
-                for (int k16 = 0; k16 < kKS / 16; ++k16)
-                  umma_f16(tmem + a * kNT, sw128_desc(asm_ + 32 * k16), sw128_desc(bsm + 32 * k16),
-                           idesc, (sbc | kk | k16) != 0);
-              }
-              umma_commit(&op_empty[s]);  // frees A and B of this stage once the MMAs finish
-              if (sbc == nsb - 1 && kk == kKSteps - 1) umma_commit(&acc_bar);
-            }
-          }
+            for (int k16 = 0; k16 < kKS / 16; ++k16)
+              umma_f16(tmem + a * kNT, sw128_desc(as + a * kATile + 32 * k16),
+                       sw128_desc(bs + 32 * k16), idesc, (ks | k16) != 0);
+          umma_commit(&a_empty[sa]);  // the A stage may be rewritten once these finish
+          umma_commit(&b_empty[sb]);  // ... and the B stage refilled
         }
+        if (!*abort) umma_commit(&acc_full);
       }
-      // ---- epilogue: TMEM -> registers -> global ----
-      wait_or_abort(&acc_bar, tcount & 1u, abort);
-      tc_fence_after();
-      const bool live = !*abort;            // warp-uniform enough: only gates stores
-      const int quad = warp & 3;            // TMEM lanes 32*quad .. 32*quad+31
-      const int colh = (warp - 1) >> 2;     // which half of the columns
-      const int trow = 32 * quad + lane;    // tile row of this thread
-      const uint32_t tbase = tmem + ((uint32_t)(32 * quad) << 16);
-      for (int c0 = colh * (kNT / 2); c0 < (colh + 1) * (kNT / 2) && c0 < t.count; c0 += 16) {
-        uint32_t g[16];
-        tmem_ld16(tbase + c0, g);
-        if (UG) {
-          uint32_t u[16];
-          tmem_ld16(tbase + kNT + c0, u);
-          const int f = t.mtile * kTM + trow;
+      // every MMA issued has finished before TMEM is released
+      umma_commit(&fin_bar);
+      mbar_wait_ns(&fin_bar, 0, kWaitNs);
+    }
+  } else {
+    // ====================== dequantise + epilogue ======================
+    const int dt = tid - 32 * kDqWarp0;
+    const int r = dt >> 1, blk = dt & 1;  // tile row, block parity within a k-step
+    const int a = r >> 7, rr = r & (kTM - 1);
+    const int quad = warp & 3;            // TMEM lanes 32*quad .. 32*quad+31
+    const int qc = (warp - kDqWarp0) >> 2;  // column quarter of the epilogue
+    // fp16 scales of the row's superblocks: 16 bytes each, one superblock ahead
+    auto row_ptr = [&](int ti) -> const uint8_t * {
+      if (ti >= ntiles) return nullptr;
+      const TcTile tn = p.tiles[ti];
+      return p.w + ((int64_t)tn.expert * p.rows_per_expert + tile_row<UG>(tn.mtile, r)) * p.row_bytes;
+    };
+    const uint8_t *rowp = row_ptr(blockIdx.x);
+    uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_nxt = sc_cur;
+    if (rowp) sc_cur = __ldg(reinterpret_cast<const uint4 *>(rowp));
+    uint32_t q = 0, tcount = 0;
+    for (int ti = blockIdx.x; ti < ntiles; ti += gridDim.x, ++tcount) {
+      const TcTile t = p.tiles[ti];
+      const uint8_t *nrowp = row_ptr(ti + gridDim.x);
+      for (int sbc = 0; sbc < nsb; ++sbc) {
+        if (sbc + 1 < nsb)
+          sc_nxt = __ldg(reinterpret_cast<const uint4 *>(rowp + (sbc + 1) * kSBBytes));
+        else if (nrowp)
+          sc_nxt = __ldg(reinterpret_cast<const uint4 *>(nrowp));
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            if (live && col < t.count) {
-              const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-              const float h = gv / (1.0f + expf(-gv)) * uv;
-              if (!(fabsf(h) <= 65504.f)) atomicOr(p.err, kErrOverflow);
-              p.h16[(int64_t)(t.row0 + col) * p.Fp + f] = __float2half_rn(h);
-            }
+        for (int kk = 0; kk < kKSteps; ++kk, ++q) {
+          const int sl = q % kLabStages;
+          wait_or_abort(&lab_full[sl], (q / kLabStages) & 1u, abort);
+          const uint4 lab = *reinterpret_cast<const uint4 *>(lab_base + sl * kLabStage + r * 32 + blk * 16);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&lab_empty[sl]);  // the labels are in registers
+          const int sa = q % kAStages;
+          if (q >= kAStages) wait_or_abort(&a_empty[sa], ((q / kAStages) - 1) & 1u, abort);
+          const uint32_t sw = kk == 0 ? sc_cur.x : kk == 1 ? sc_cur.y : kk == 2 ? sc_cur.z : sc_cur.w;
+          const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)(blk ? sw >> 16 : sw & 0xFFFF)));
+          const uint32_t ww[4] = {lab.x, lab.y, lab.z, lab.w};
+          uint8_t *arow = a_base + sa * kAStage + a * kATile + rr * 128;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {  // 8 weights: chunk 4*blk + cc of the row's k-step
+            const int c = 4 * blk + cc;
+            uint32_t b0, b1, h0, h1, h2, h3;
+            iq4_decode8_biased(ww[cc], b0, b1);
+            codes_to_half(b0, d2, h0, h1);
+            codes_to_half(b1, d2, h2, h3);
+            *reinterpret_cast<uint4 *>(arow + ((c ^ (rr & 7)) << 4)) = make_uint4(h0, h1, h2, h3);
           }
-        } else {
-          const int n = t.mtile * kTM + trow;
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // A tile -> tensor core
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[sa]);
+        }
+        sc_cur = sc_nxt;
+      }
+      rowp = nrowp;
+
+      // ---- epilogue: TMEM -> registers -> global ----
+      wait_or_abort(&acc_full, tcount & 1u, abort);
+      tc_fence_after();
+      // Down: the tile's route tokens and weights, read once into the first
+      // A stage -- every MMA of the tile has finished, and no dequantiser
+      // writes an A stage again before the barrier closing this epilogue.
+      int *ep_tok = reinterpret_cast<int *>(a_base);
+      float *ep_w = reinterpret_cast<float *>(a_base + kNT * sizeof(int));
+      if (!UG) {
+        for (int j = dt; j < t.count; j += kDq) {
+          ep_tok[j] = p.route_token[t.row0 + j];
+          ep_w[j] = p.route_weight[t.row0 + j];
+        }
+        named_sync(1, kDq);
+      }
+      const bool live = __shfl_sync(0xffffffffu, *abort == 0 ? 1 : 0, 0) != 0;
+      const int trow = 32 * quad + lane;  // accumulator row (TMEM lane) of this thread
+      const uint32_t tbase = tmem + ((uint32_t)(32 * quad) << 16);
+      if (live) {
+        for (int c0 = qc * (kNT / 4); c0 < (qc + 1) * (kNT / 4) && c0 < t.count; c0 += 16) {
+          uint32_t g[16], u[16];
+          tmem_ld16_nowait(tbase + c0, g);
+          tmem_ld16_nowait(tbase + kNT + c0, u);
+          tmem_wait_ld();
+          if (UG) {
+            const int f = t.mtile * kTM + trow;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            if (live && col < t.count && n < p.H) {
-              const int pos = t.row0 + col;
-              atomicAdd(p.out_acc + (int64_t)p.route_token[pos] * p.H + n,
-                        p.route_weight[pos] * __uint_as_float(g[j]));
+            for (int j = 0; j < 16; ++j) {
+              const int col = c0 + j;
+              if (col < t.count) {
+                const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
+                // silu(g) = g / (1 + e^-g); e^-g capped at e^80 keeps the
+                // fast divide in range (the quotient is ~0 there anyway)
+                const float h = __fdividef(gv, 1.0f + __expf(fminf(-gv, 80.0f))) * uv;
+                if (!(fabsf(h) <= 65504.f)) atomicOr(p.err, kErrOverflow);
+                p.h16[(int64_t)(t.row0 + col) * p.Fp + f] = __float2half_rn(h);
+              }
+            }
+          } else {
+            const int n0 = t.mtile * kRowsTile + trow, n1 = n0 + kTM;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int col = c0 + j;
+              if (col < t.count) {
+                const float wgt = ep_w[col];
+                float *orow = p.out_acc + (int64_t)ep_tok[col] * p.H;
+                if (n0 < p.H) atomicAdd(orow + n0, wgt * __uint_as_float(g[j]));
+                if (n1 < p.H) atomicAdd(orow + n1, wgt * __uint_as_float(u[j]));
+              }
             }
           }
         }
       }
       tc_fence_before();
-      ++tcount;
-    }
-    // all MMAs this thread issued have finished before TMEM is released
-    if (ct == 0) {
-      umma_commit(&fin_bar);
-      mbar_wait_ns(&fin_bar, 0, kWaitNs);
+      if (!UG) named_sync(1, kDq);  // ep_tok / ep_w read by all before A is rewritten
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty);
     }
   }
 
@@ -385,30 +426,58 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 }
 
 // Tile lists from the route plan: for every expert with routes, route tiles
-// of <= 256 and, per route tile, every 128-row weight tile.  Lane 0 walks
-// the (expert, route tile) pairs; the warp writes their weight tiles.
-__global__ void build_tiles_kernel(const int *offsets, const int *active, int n_slots_idx,
-                                   int ug_mtiles, int dn_mtiles, TcTile *ug, TcTile *dn,
-                                   int *counts, int max_ug, int max_dn) {
-  const int lane = threadIdx.x;
+// of <= 256 and, per route tile, every weight tile (Fp/128 up/gate tiles,
+// Hp/256 down tiles), expert by expert in the order of the active list.
+// One block: thread i counts the route tiles of active expert i, a block
+// scan places them, and each thread writes its own expert's tiles.
+constexpr int kTileThreads = 256;
+__global__ void __launch_bounds__(kTileThreads)
+    build_tiles_kernel(const int *offsets, const int *active, int n_slots_idx, int ug_mtiles,
+                       int dn_mtiles, TcTile *ug, TcTile *dn, int *counts, int max_ug, int max_dn) {
+  __shared__ int warp_sum[kTileThreads / 32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int n_act = active[n_slots_idx];
-  int nu = 0, nd = 0;
-  for (int i = 0; i < n_act; ++i) {
-    const int e = active[i];
-    const int beg = offsets[e], cnt = offsets[e + 1] - beg;
-    for (int n0 = 0; n0 < cnt; n0 += kNT) {
-      const int c = min(kNT, cnt - n0);
-      for (int m = lane; m < ug_mtiles; m += 32)
-        if (nu + m < max_ug) ug[nu + m] = TcTile{e, m, beg + n0, c};
-      for (int m = lane; m < dn_mtiles; m += 32)
-        if (nd + m < max_dn) dn[nd + m] = TcTile{e, m, beg + n0, c};
-      nu = min(nu + ug_mtiles, max_ug);
-      nd = min(nd + dn_mtiles, max_dn);
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int i0 = 0; i0 < n_act; i0 += kTileThreads) {
+    const int i = i0 + tid;
+    int e = 0, beg = 0, cnt = 0, nrt = 0;
+    if (i < n_act) {
+      e = active[i];
+      beg = offsets[e];
+      cnt = offsets[e + 1] - beg;
+      nrt = (cnt + kNT - 1) / kNT;
     }
+    int incl = nrt;  // inclusive scan within the warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    if (lane == 31) warp_sum[wid] = incl;
+    __syncthreads();
+    int base = carry;
+    for (int w = 0; w < wid; ++w) base += warp_sum[w];
+    base += incl - nrt;  // route tiles before this expert's
+    for (int j = 0; j < nrt; ++j) {
+      const int c = min(kNT, cnt - j * kNT);
+      for (int m = 0; m < ug_mtiles; ++m) {
+        const int idx = (base + j) * ug_mtiles + m;
+        if (idx < max_ug) ug[idx] = TcTile{e, m, beg + j * kNT, c};
+      }
+      for (int m = 0; m < dn_mtiles; ++m) {
+        const int idx = (base + j) * dn_mtiles + m;
+        if (idx < max_dn) dn[idx] = TcTile{e, m, beg + j * kNT, c};
+      }
+    }
+    __syncthreads();
+    if (tid == kTileThreads - 1) carry = base + nrt;
+    __syncthreads();
   }
-  if (lane == 0) {
-    counts[0] = nu;
-    counts[1] = nd;
+  if (tid == 0) {
+    counts[0] = min(carry * ug_mtiles, max_ug);
+    counts[1] = min(carry * dn_mtiles, max_dn);
   }
 }
 
@@ -485,41 +554,41 @@ cudaError_t encode_2d(CUtensorMap *map, CUtensorMapDataType dt, void *base, uint
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool UG>
 size_t tc_smem() {
-  constexpr int NA = UG ? 2 : 1;
-  return 1024 + (size_t)kOpStages * (NA * kATile + kBTile) + (size_t)kRawStages * NA * kTM * kSBBytes;
+  return 1024 + (size_t)kAStages * kAStage + (size_t)kBStages * kBTile + (size_t)kLabStages * kLabStage;
 }
 
 }  // namespace
 
 int tc_max_tiles(const Layer &L, bool up_gate) {
-  const int64_t n_tiles = (int64_t)L.max_routes / kNT + L.E + L.S;
-  return (int)(n_tiles * (up_gate ? L.Fp / kTM : L.Hp / kTM));
+  const int64_t route_tiles = (int64_t)L.max_routes / kNT + L.E + L.S;
+  return (int)(route_tiles * (up_gate ? L.Fp / kTM : L.Hp / kRowsTile));
 }
 
 cudaError_t tc_prepare(Layer &L) {
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
-  e = encode_2d(&L.map_gu_raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.gu, (uint64_t)L.gu_row_bytes,
-                (uint64_t)(L.E + L.S) * 2 * L.Fp, (uint64_t)L.gu_row_bytes, kSBBytes, 64,
+  // labels of one k-step: 32 bytes of each of 64 (up/gate: one gate/up
+  // group) or 256 (down) consecutive rows
+  e = encode_2d(&L.map_gu_lab, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.gu, (uint64_t)L.gu_row_bytes,
+                (uint64_t)(L.E + L.S) * 2 * L.Fp, (uint64_t)L.gu_row_bytes, 32, kGroupRows,
                 CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e == cudaSuccess)
-    e = encode_2d(&L.map_dn_raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.dn, (uint64_t)L.dn_row_bytes,
-                  (uint64_t)(L.E + L.S) * L.Hp, (uint64_t)L.dn_row_bytes, kSBBytes, kTM,
+    e = encode_2d(&L.map_dn_lab, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.dn, (uint64_t)L.dn_row_bytes,
+                  (uint64_t)(L.E + L.S) * L.Hp, (uint64_t)L.dn_row_bytes, 32, kRowsTile,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e == cudaSuccess)
     e = encode_2d(&L.map_x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, L.x16, (uint64_t)L.Hp,
-                  (uint64_t)L.max_routes, (uint64_t)L.Hp * 2, kKS, kNT, CU_TENSOR_MAP_SWIZZLE_128B);
+                (uint64_t)L.max_routes, (uint64_t)L.Hp * 2, kKS, kNT, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e == cudaSuccess)
     e = encode_2d(&L.map_h16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, L.h16, (uint64_t)L.Fp,
                   (uint64_t)L.max_routes, (uint64_t)L.Fp * 2, kKS, kNT, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(grouped_gemm_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tc_smem<true>());
+                           (int)tc_smem());
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(grouped_gemm_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tc_smem<false>());
+                             (int)tc_smem());
   if (e == cudaSuccess && g_sms_tc == 0) {
     int dev = 0;
     e = cudaGetDevice(&dev);
@@ -532,9 +601,10 @@ cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int 
                               cudaStream_t stream) {
   const int max_rows = T * L.k + L.S * T;
   // tile lists
-  build_tiles_kernel<<<1, 32, 0, stream>>>(L.offsets, L.active, L.E + L.S, L.Fp / kTM, L.Hp / kTM,
-                                           L.tiles_ug, L.tiles_dn, L.tile_counts,
-                                           tc_max_tiles(L, true), tc_max_tiles(L, false));
+  build_tiles_kernel<<<1, kTileThreads, 0, stream>>>(L.offsets, L.active, L.E + L.S, L.Fp / kTM,
+                                                     L.Hp / kRowsTile, L.tiles_ug, L.tiles_dn,
+                                                     L.tile_counts, tc_max_tiles(L, true),
+                                                     tc_max_tiles(L, false));
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -559,18 +629,22 @@ cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int 
   p.H = L.H;
   p.Hp = L.Hp;
   p.Fp = L.Fp;
-  p.gu_rows_per_expert = 2 * (int64_t)L.Fp;
-  p.dn_rows_per_expert = L.Hp;
   // up/gate + SwiGLU
   p.tiles = L.tiles_ug;
   p.n_tiles = L.tile_counts;
-  grouped_gemm_tc<true><<<g_sms_tc, kThreadsTC, tc_smem<true>(), stream>>>(p, L.map_gu_raw, L.map_x16);
+  p.w = L.gu;
+  p.row_bytes = L.gu_row_bytes;
+  p.rows_per_expert = 2 * (int64_t)L.Fp;
+  grouped_gemm_tc<true><<<g_sms_tc, kThreadsTC, tc_smem(), stream>>>(p, L.map_x16, L.map_gu_lab);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // down + weighted scatter
   p.tiles = L.tiles_dn;
   p.n_tiles = L.tile_counts + 1;
-  grouped_gemm_tc<false><<<g_sms_tc, kThreadsTC, tc_smem<false>(), stream>>>(p, L.map_dn_raw, L.map_h16);
+  p.w = L.dn;
+  p.row_bytes = L.dn_row_bytes;
+  p.rows_per_expert = L.Hp;
+  grouped_gemm_tc<false><<<g_sms_tc, kThreadsTC, tc_smem(), stream>>>(p, L.map_h16, L.map_dn_lab);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -6,7 +6,8 @@
 //   - small T: one warp per expert streams its Wr row once with 128-bit loads
 //     and serves every token (Wr is read from HBM exactly once);
 //   - large T: a 32-token x 64-expert register-tiled SIMT product through
-//     shared memory (Wr rows are reused by 32 tokens per tile).
+//     shared memory (Wr rows are reused by 32 tokens per tile), the next K
+//     chunk's global loads overlapping the current chunk's FMAs.
 // Step 2 (selection): one warp per token; the k largest logits are taken in
 // descending order (sigmoid is monotone, so this is the order of the
 // scores), equal logits going to the lower id; s = 1/(1+e^-l) for the k
@@ -83,51 +84,71 @@ __global__ void __launch_bounds__(256) router_logits_small(const XT *__restrict_
 
 constexpr int kTM = 32, kTN = 64, kKC = 32;
 
+// 32 tokens x 64 experts per CTA, 256 threads of 2 tokens x 4 experts.  The
+// next K chunk's x and Wr values are loaded into registers while the current
+// chunk is multiplied out of shared memory, so the global latency is paid
+// once, not once per chunk.  x is kept token-major and Wr transposed to
+// k-major in shared memory: every inner step is two 16-byte x reads
+// (broadcast within the warp) and four 16-byte Wr reads for 32 FMAs.
 template <typename XT>
 __global__ void __launch_bounds__(256) router_logits_tiled(const XT *__restrict__ x, int T, int H,
                                                            const float *__restrict__ wr, int E,
                                                            const float *__restrict__ bias,
                                                            int64_t bstride,
                                                            float *__restrict__ logits) {
-  __shared__ float xs[kKC][kTM + 4];
+  __shared__ __align__(16) float xs[kTM][kKC + 4];
   __shared__ __align__(16) float ws[kKC][kTN + 4];
   const int tid = threadIdx.x;
-  const int ty = tid >> 4, tx = tid & 15;  // 16 x 16 threads: 2 tokens x 4 experts each
+  const int ty = tid >> 4, tx = tid & 15;  // tokens 2ty, 2ty+1; experts 4tx .. 4tx+3
   const int t0 = blockIdx.x * kTM, e0 = blockIdx.y * kTN;
+  // load mapping: x token lt, k offset lk (4 values); Wr expert le, k offset lw (8 values)
+  const int lt = tid >> 3, lk = (tid & 7) * 4;
+  const int le = tid & 63, lw = (tid >> 6) * 8;
+  const bool xv_ok = t0 + lt < T, wv_ok = e0 + le < E;
+  const XT *xp = x + (int64_t)(t0 + lt) * H + lk;
+  const float *wp = wr + (int64_t)(e0 + le) * H + lw;
+  float4 xr = make_float4(0.f, 0.f, 0.f, 0.f), wr0 = xr, wr1 = xr;
+  if (xv_ok) xr = load_x4<XT>(xp);
+  if (wv_ok) {
+    wr0 = *reinterpret_cast<const float4 *>(wp);
+    wr1 = *reinterpret_cast<const float4 *>(wp + 4);
+  }
   float acc[2][4] = {};
   for (int k0 = 0; k0 < H; k0 += kKC) {
-    {  // x tile: 32 tokens x 32 k, 4 per thread
-      const int tt = tid >> 3, kk = (tid & 7) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t0 + tt < T) v = load_x4<XT>(x + (int64_t)(t0 + tt) * H + k0 + kk);
-      xs[kk + 0][tt] = v.x;
-      xs[kk + 1][tt] = v.y;
-      xs[kk + 2][tt] = v.z;
-      xs[kk + 3][tt] = v.w;
+    *reinterpret_cast<float4 *>(&xs[lt][lk]) = xr;
+    ws[lw + 0][le] = wr0.x;
+    ws[lw + 1][le] = wr0.y;
+    ws[lw + 2][le] = wr0.z;
+    ws[lw + 3][le] = wr0.w;
+    ws[lw + 4][le] = wr1.x;
+    ws[lw + 5][le] = wr1.y;
+    ws[lw + 6][le] = wr1.z;
+    ws[lw + 7][le] = wr1.w;
+    __syncthreads();
+    if (k0 + kKC < H) {  // next chunk in flight during this one's FMAs
+      if (xv_ok) xr = load_x4<XT>(xp + k0 + kKC);
+      if (wv_ok) {
+        wr0 = *reinterpret_cast<const float4 *>(wp + k0 + kKC);
+        wr1 = *reinterpret_cast<const float4 *>(wp + k0 + kKC + 4);
+      }
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {  // Wr tile: 64 experts x 32 k, 8 per thread
-      const int ee = (tid >> 3) + 32 * h, kk = (tid & 7) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e0 + ee < E) v = *reinterpret_cast<const float4 *>(wr + (int64_t)(e0 + ee) * H + k0 + kk);
-      ws[kk + 0][ee] = v.x;
-      ws[kk + 1][ee] = v.y;
-      ws[kk + 2][ee] = v.z;
-      ws[kk + 3][ee] = v.w;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kKC; ++kk) {
-      const float a0 = xs[kk][ty * 2], a1 = xs[kk][ty * 2 + 1];
-      const float4 b = *reinterpret_cast<const float4 *>(&ws[kk][tx * 4]);
-      acc[0][0] = fmaf(a0, b.x, acc[0][0]);
-      acc[0][1] = fmaf(a0, b.y, acc[0][1]);
-      acc[0][2] = fmaf(a0, b.z, acc[0][2]);
-      acc[0][3] = fmaf(a0, b.w, acc[0][3]);
-      acc[1][0] = fmaf(a1, b.x, acc[1][0]);
-      acc[1][1] = fmaf(a1, b.y, acc[1][1]);
-      acc[1][2] = fmaf(a1, b.z, acc[1][2]);
-      acc[1][3] = fmaf(a1, b.w, acc[1][3]);
+    for (int kk = 0; kk < kKC; kk += 4) {
+      const float4 a0 = *reinterpret_cast<const float4 *>(&xs[2 * ty][kk]);
+      const float4 a1 = *reinterpret_cast<const float4 *>(&xs[2 * ty + 1][kk]);
+      const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 b = *reinterpret_cast<const float4 *>(&ws[kk + j][tx * 4]);
+        acc[0][0] = fmaf(av0[j], b.x, acc[0][0]);
+        acc[0][1] = fmaf(av0[j], b.y, acc[0][1]);
+        acc[0][2] = fmaf(av0[j], b.z, acc[0][2]);
+        acc[0][3] = fmaf(av0[j], b.w, acc[0][3]);
+        acc[1][0] = fmaf(av1[j], b.x, acc[1][0]);
+        acc[1][1] = fmaf(av1[j], b.y, acc[1][1]);
+        acc[1][2] = fmaf(av1[j], b.z, acc[1][2]);
+        acc[1][3] = fmaf(av1[j], b.w, acc[1][3]);
+      }
     }
     __syncthreads();
   }
