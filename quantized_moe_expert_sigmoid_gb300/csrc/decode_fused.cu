@@ -59,7 +59,6 @@ constexpr int kH4 = 4;     // float4 loads in flight per thread when gathering h
 constexpr uint32_t kPollLimit = 1u << 24;
 constexpr uint32_t kSpinLimit = 1u << 21;
 constexpr int kBarConsumers = 1;  // named barrier ids (0 is __syncthreads)
-constexpr int kBarPair0 = 2;      // 2..9: gate/up warp pairs
 
 struct Params {
   Layer L;
@@ -114,7 +113,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
   __shared__ int sel_id[kFusedMaxTokens][8];
   __shared__ float sel_w[kFusedMaxTokens][8];
   __shared__ float red[kConsumerWarps][TT];
-  __shared__ float up_part[2][8][TT];  // [item parity][output][route]
   __shared__ float rowacc[kMaxRowsCta][TT];
 
   const Layer &L = p.L;
@@ -194,6 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     int issued = 0;
     if (lane == 0) {
       for (; issued < n_shared_items && issued < nst; ++issued) issue(issued);
+      if (S && nrows > 0)  // the shared expert's W_down rows of this CTA, known before routing
+        bulk_prefetch_l2(L.dn + (int64_t)E * L.dn_expert_bytes + (int64_t)n0 * db, (uint32_t)(nrows * db));
       if (do_route && p.wr_rows_smem > 0) {  // router rows -> last stage (no shared item uses it)
         int nr = 0;
         for (int e = c; e < E; e += G) ++nr;
@@ -231,31 +231,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             const float l = e < E ? __ldcg(&L.logits[(int64_t)t * E + e]) : -FLT_MAX;
             v[i] = (l == l) ? l : -FLT_MAX;  // NaN never wins
           }
+          // k rounds of a warp arg-max on order-preserving integer keys:
+          // one redux for the largest key, one for the lowest expert id
+          // holding it (equal logits go to the lower id)
+          uint32_t key[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) key[i] = lane + 32 * i < E ? float_order_key(v[i]) : 0u;
           unsigned taken = 0;
           float ssum = 0.f, my_s = 0.f;
           int my_id = 0;
           for (int j = 0; j < K; ++j) {
-            float best = -INFINITY;
-            int bid = 0x7fffffff;
+            uint32_t lk = 0;
+            int li = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int e = lane + 32 * i;
-              if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < bid))) {
-                best = v[i];
-                bid = e;
+            for (int i = 0; i < 8; ++i)
+              if (!((taken >> i) & 1u) && key[i] > lk) {
+                lk = key[i];
+                li = i;
               }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-              const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-              if (ob > best || (ob == best && oid < bid)) {
-                best = ob;
-                bid = oid;
-              }
-            }
+            const uint32_t m = __reduce_max_sync(0xffffffffu, lk);
+            const int bid =
+                (int)__reduce_min_sync(0xffffffffu, lk == m ? (uint32_t)(lane + 32 * li) : 0xffffffffu);
             if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-            const float sg = 1.0f / (1.0f + expf(-best));
+            const float sg = 1.0f / (1.0f + expf(-float_from_order_key(m)));
             ssum += sg;
             if (lane == j) {
               my_id = bid;
@@ -362,10 +360,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(&plan_bar);  // release: the tables above become visible to the waiters
-      for (int i = issued; i < n_items; ++i) {
+      int i = issued;
+      for (; i < n_items && i < nst; ++i) issue(i);  // stages never used yet
+      // this CTA's W_down rows of every routed expert into L2 now: their
+      // ring stages free up only as the up/gate items are consumed
+      for (int a = S; a < n_ex && nrows > 0; ++a)
+        bulk_prefetch_l2(L.dn + (int64_t)ex_id[a] * L.dn_expert_bytes + (int64_t)n0 * db,
+                         (uint32_t)(nrows * db));
+      for (; i < n_items; ++i) {
         const int s = i % nst;
-        if (i >= nst &&
-            !mbar_wait_bounded(&empty_bar[s], (uint32_t)((i / nst) - 1) & 1u, kPollLimit)) {
+        if (!mbar_wait_bounded(&empty_bar[s], (uint32_t)((i / nst) - 1) & 1u, kPollLimit)) {
           atomicOr(&status, 2);
           break;
         }
@@ -483,44 +487,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     }
     named_sync(kBarConsumers, kConsumers);
 
-    // One up/gate item: warp w works on output f0 + (w & 7), on its gate row
-    // (w < 8) or its up row (w >= 8); lanes split the row's 16-weight
-    // half-blocks.  The pair meets at a named barrier for SwiGLU.
+    // One up/gate item (gate rows of up to fpi outputs in the stage's first
+    // half, their up rows in the second) is taken by one half of the
+    // consumer warps -- items alternate between the halves, so two items
+    // are in work at once.  Warp w computes both rows of output f0 + (w & 7):
+    // every activation load serves the gate and the up row, and SwiGLU is
+    // applied inside the warp.  Each of the 8 warps arrives twice on the
+    // stage's "empty" barrier (its count is the 16 consumer warps).
     auto process_upgate = [&](int i) {
       const Item it = items[i];
       const int s = i % nst;
-      if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(i / nst) & 1u, kPollLimit)) atomicOr(&status, 2);
+      if (!mbar_wait_sleep(&full_bar[s], (uint32_t)(i / nst) & 1u, kPollLimit, 32)) atomicOr(&status, 2);
       const int rs = ex_rs[it.a], nr = ex_rs[it.a + 1] - rs;
-      const int fl = warp & 7, is_up = warp >> 3;
-      float acc[TT];
+      const int fl = warp & 7;
+      float accg[TT], accu[TT];
 #pragma unroll
-      for (int r = 0; r < TT; ++r) acc[r] = 0.f;
+      for (int r = 0; r < TT; ++r) accg[r] = accu[r] = 0.f;
       if (fl < it.count) {
-        const uint8_t *row = ring + (size_t)s * kStage + (size_t)(is_up * p.fpi + fl) * rb;
+        const uint8_t *rowg = ring + (size_t)s * kStage + (size_t)fl * rb;
+        const uint8_t *rowu = rowg + (size_t)p.fpi * rb;
         int toks[TT];
 #pragma unroll
         for (int r = 0; r < TT; ++r) toks[r] = r < nr ? r_tok[rs + r] : 0;
         if constexpr (NP > 0) {
           constexpr int kHp = NP * 512, kHb = NP * 16;
-          const uint8_t *wl = row + (lane >> 4) * kSBBytes + 16 + ((lane >> 1) & 7) * 16 + (lane & 1) * 8;
-          const uint8_t *dl = row + (lane >> 4) * kSBBytes + ((lane >> 1) & 7) * 2;
+          const int lofs = (lane >> 4) * kSBBytes + 16 + ((lane >> 1) & 7) * 16 + (lane & 1) * 8;
+          const int dofs = (lane >> 4) * kSBBytes + ((lane >> 1) & 7) * 2;
           const int b0 = lane >> 1;
 #pragma unroll
           for (int k = 0; k < NP; ++k) {
-            const uint2 q = *reinterpret_cast<const uint2 *>(wl + 2 * kSBBytes * k);
-            const float d = __half2float(*reinterpret_cast<const __half *>(dl + 2 * kSBBytes * k));
-            uint32_t c0, c1, c2, c3;
-            iq4_decode8(q.x, c0, c1);
-            iq4_decode8(q.y, c2, c3);
+            const uint2 qg = *reinterpret_cast<const uint2 *>(rowg + lofs + 2 * kSBBytes * k);
+            const uint2 qu = *reinterpret_cast<const uint2 *>(rowu + lofs + 2 * kSBBytes * k);
+            const float dg = __half2float(*reinterpret_cast<const __half *>(rowg + dofs + 2 * kSBBytes * k));
+            const float du = __half2float(*reinterpret_cast<const __half *>(rowu + dofs + 2 * kSBBytes * k));
+            uint32_t g0, g1, g2, g3, u0, u1, u2, u3;
+            iq4_decode8(qg.x, g0, g1);
+            iq4_decode8(qg.y, g2, g3);
+            iq4_decode8(qu.x, u0, u1);
+            iq4_decode8(qu.y, u2, u3);
 #pragma unroll
             for (int r = 0; r < TT; ++r) {
               if (r < nr) {
                 const int16_t *xr = xq + toks[r] * kHp + lane * 16 + 512 * k;
                 const uint4 xa = *reinterpret_cast<const uint4 *>(xr);
                 const uint4 xb = *reinterpret_cast<const uint4 *>(xr + 8);
-                const int s0 = dot8_dp2a(c0, c1, xa, 0);
-                const int s1 = dot8_dp2a(c2, c3, xb, 0);
-                acc[r] = fmaf((float)(s0 + s1), d * sx[toks[r] * kHb + b0 + 16 * k], acc[r]);
+                const float sxv = sx[toks[r] * kHb + b0 + 16 * k];
+                const int sg = dot8_dp2a(g0, g1, xa, 0) + dot8_dp2a(g2, g3, xb, 0);
+                const int su = dot8_dp2a(u0, u1, xa, 0) + dot8_dp2a(u2, u3, xb, 0);
+                accg[r] = fmaf((float)sg, dg * sxv, accg[r]);
+                accu[r] = fmaf((float)su, du * sxv, accu[r]);
               }
             }
           }
@@ -528,49 +543,52 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
 #pragma unroll 2
           for (int pos = lane; pos < Hp / 16; pos += 32) {
             const int b = pos >> 1, sb = b >> 3, j = b & 7, half = pos & 1;
-            const uint8_t *ps = row + sb * kSBBytes;
-            const float d = __half2float(reinterpret_cast<const __half *>(ps)[j]);
-            const uint2 q = *reinterpret_cast<const uint2 *>(ps + 16 + j * 16 + half * 8);
-            uint32_t c0, c1, c2, c3;
-            iq4_decode8(q.x, c0, c1);
-            iq4_decode8(q.y, c2, c3);
+            const uint8_t *pg = rowg + sb * kSBBytes, *pu = rowu + sb * kSBBytes;
+            const float dg = __half2float(reinterpret_cast<const __half *>(pg)[j]);
+            const float du = __half2float(reinterpret_cast<const __half *>(pu)[j]);
+            const uint2 qg = *reinterpret_cast<const uint2 *>(pg + 16 + j * 16 + half * 8);
+            const uint2 qu = *reinterpret_cast<const uint2 *>(pu + 16 + j * 16 + half * 8);
+            uint32_t g0, g1, g2, g3, u0, u1, u2, u3;
+            iq4_decode8(qg.x, g0, g1);
+            iq4_decode8(qg.y, g2, g3);
+            iq4_decode8(qu.x, u0, u1);
+            iq4_decode8(qu.y, u2, u3);
 #pragma unroll
             for (int r = 0; r < TT; ++r) {
               if (r < nr) {
                 const uint4 *xp4 = reinterpret_cast<const uint4 *>(xq + (size_t)toks[r] * Hp + pos * 16);
                 const uint4 xa = xp4[0], xb = xp4[1];
-                const int s0 = dot8_dp2a(c0, c1, xa, 0);
-                const int s1 = dot8_dp2a(c2, c3, xb, 0);
-                acc[r] = fmaf((float)(s0 + s1), d * sx[(size_t)toks[r] * hb + b], acc[r]);
+                const float sxv = sx[(size_t)toks[r] * hb + b];
+                const int sg = dot8_dp2a(g0, g1, xa, 0) + dot8_dp2a(g2, g3, xb, 0);
+                const int su = dot8_dp2a(u0, u1, xa, 0) + dot8_dp2a(u2, u3, xb, 0);
+                accg[r] = fmaf((float)sg, dg * sxv, accg[r]);
+                accu[r] = fmaf((float)su, du * sxv, accu[r]);
               }
             }
           }
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[s]);  // this warp is done with the stage
-      // The pair meets at every item, also one that has no output f0 + fl:
-      // up_part is double-buffered by item parity, so the up warp may only
-      // write item i + 2's value after the gate warp has read item i's,
-      // which the barrier of item i + 1 guarantees.
-      float v[TT];
+      if (lane == 0) mbar_arrive_cnt(&empty_bar[s], 2);  // for this warp and its idle twin
+      if (fl < it.count) {
 #pragma unroll
-      for (int r = 0; r < TT; ++r) v[r] = r < nr ? warp_sum(acc[r]) : 0.f;
-      if (fl < it.count && is_up && lane == 0)
-        for (int r = 0; r < nr; ++r) up_part[i & 1][fl][r] = v[r];
-      named_sync(kBarPair0 + fl, 64);
-      if (fl < it.count && !is_up && lane == 0)
-        for (int r = 0; r < nr; ++r) {
-          const float g = v[r], u = up_part[i & 1][fl][r];
-          L.h32[(int64_t)(rs + r) * Fp + it.f0 + fl] = g / (1.0f + expf(-g)) * u;
+        for (int r = 0; r < TT; ++r) {
+          if (r < nr) {
+            const float g = warp_sum(accg[r]), u = warp_sum(accu[r]);
+            if (lane == 0) L.h32[(int64_t)(rs + r) * Fp + it.f0 + fl] = g / (1.0f + expf(-g)) * u;
+          }
         }
+      }
     };
 
     int i = 0;
-    for (; i < n_shared_items; ++i) process_upgate(i);
-    if (!mbar_wait_bounded(&plan_bar, 0, kPollLimit)) atomicOr(&status, 2);
+    const int my_half = warp >> 3;  // up/gate items alternate between the warp halves
+    for (; i < n_shared_items; ++i)
+      if ((i & 1) == my_half) process_upgate(i);
+    if (!mbar_wait_sleep(&plan_bar, 0, kPollLimit, 128)) atomicOr(&status, 2);
     if (!(status & 1)) {
-      for (; i < n_items && items[i].kind == 0; ++i) process_upgate(i);
+      for (; i < n_items && items[i].kind == 0; ++i)
+        if ((i & 1) == my_half) process_upgate(i);
 
       // ---- every CTA's h written ----
       named_sync(kBarConsumers, kConsumers);
@@ -775,7 +793,10 @@ bool plan_fused(const Layer &L, int T, FusedPlan &fp) {
   const size_t fixed = (size_t)T * L.Hp * 2 + (size_t)T * (L.Hp / 32) * 4;
   const size_t limit = smem_limit_fused();
   if (fixed + (size_t)T * per_route + 3 * (size_t)kStage > limit) return false;
-  fp.nstage = (int)std::min<size_t>(kMaxStages, (limit - fixed - (size_t)T * per_route) / kStage);
+  // an even number of stages: up/gate items alternate between the two
+  // consumer-warp halves, and a half's parity wait on a stage is only exact
+  // when the stage's previous use was that half's too
+  fp.nstage = (int)std::min<size_t>(kMaxStages, (limit - fixed - (size_t)T * per_route) / kStage) & ~1;
   const size_t left = limit - fixed - (size_t)fp.nstage * kStage;
   fp.hq_cap = (int)std::min<size_t>((size_t)T * (L.k + L.S), left / per_route);
   fp.smem = fixed + (size_t)fp.nstage * kStage + (size_t)fp.hq_cap * per_route;
