@@ -43,7 +43,8 @@ def parse():
     p.add_argument("--steps", type=int, default=65536)
     p.add_argument("--warmup", type=int, default=64)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="decode1", choices=["decode1", "decode64", "prefill4096"])
+    p.add_argument("--workload", default="decode1",
+                   choices=["decode1", "decode64", "prefill4096", "trunk38_t1", "trunk38_t16"])
     p.add_argument("--layers", type=int, default=16, help="resident layers the steps rotate over")
     p.add_argument("--graph-steps", type=int, default=32)
     p.add_argument("--e2e-steps", type=int, default=2000)
@@ -54,9 +55,26 @@ def parse():
 
 METRIC = "MoE-layer tokens/s (expert-weight HBM GB/s as fraction of GB300 peak)"
 
+# DRAM bytes (read + write) per launch of each workload's dominant kernel,
+# from the ncu captures summarised in profiles/ (set to None when the kernel
+# changes after its capture).
+NCU_TRAFFIC = {
+    "decode1": 32_002_560,        # decode_fused_kernel<1,7,64>: profiles/decode_fused_kernel_decode1.md
+    "prefill4096": 456_457_984,   # grouped_gemm_tc<up/gate>: profiles/grouped_gemm_tc_prefill4096.md
+}
+
 
 def bench_config(args, wl, world):
     T = wl.T
+    if wl.n_layers > 1:
+        G = max(1, min(args.graph_steps, args.steps, 8))
+        return wl.n_layers, 16, G, {
+            "workload": wl.name, "tokens_per_step": T, "layers": wl.n_layers, "hidden": wl.H,
+            "experts": wl.E, "top_k": wl.k, "expert_ffn": wl.F, "shared_experts": 1,
+            "parallelism": f"replicas x{world}",
+            "l2": f"{wl.n_layers} resident layers ({wl.n_layers * 403.5 / 1000:.1f} GB of weights, "
+                  "far larger than L2), 16 rotating inputs",
+            "graph_steps": G}
     NL = args.layers if T < 64 else max(1, min(args.layers, 2))
     NX = 64 if T < 64 else 2
     G = max(1, min(args.graph_steps, args.steps))
@@ -139,6 +157,10 @@ def cpu_baseline(wl_name, seconds):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
+    if wl.n_layers > 1:  # a token crosses every layer of the trunk (plus an RMSNorm each)
+        return {"value": done / el / wl.n_layers, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                "sample": f"{done} single-token calls of one layer of the {wl_name} trunk "
+                          f"({el:.1f} s, fp64, 1 thread), scaled by its {wl.n_layers} layers"}
     return {"value": done / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{done} single-token layer calls of the {wl_name} workload ({el:.1f} s, fp64, 1 thread)"}
 
@@ -216,6 +238,14 @@ def run_ours(args, rank, world, local_rank):
         return g
 
     reps, rem = divmod(args.steps, G)
+    # the batched path has several kernels per call: time its stages with
+    # CUDA events recorded inside the graph (event-record nodes refreshed by
+    # every replay), so the dominant kernel's own duration is measured in the
+    # timed region
+    staged = T > 8
+    if staged:
+        for L in layers:
+            moe.moe_layer_enable_timing(L.handle, G)
     launches0 = moe.moe_launch_count()
     g_main = capture(G, 0) if reps else None
     launches_per_graph = moe.moe_launch_count() - launches0
@@ -253,6 +283,15 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.all_reduce(t_ms, op=torch.distributed.ReduceOp.MAX)
     ms = float(t_ms.item())
     steps = reps * G + rem
+    stage_ms = None
+    if staged:  # per-stage means over the calls of the last replay(s)
+        rows = [r for L in layers for r in moe.moe_layer_stage_times(L.handle, G)]
+        stage_ms = {name: statistics.fmean(r[i] for r in rows) for i, name in enumerate(moe.STAGES)}
+        # the events stay bound to the graphs' nodes: drop both before any
+        # eager call on these layers
+        del g_main, g_rem
+        for L in layers:
+            moe.moe_layer_enable_timing(L.handle, 0)
     ms_per_step = ms / steps
     gpu_launches = reps * launches_per_graph + launches_rem
 
@@ -300,6 +339,29 @@ def run_ours(args, rank, world, local_rank):
         hbm_peak, peak_src = 6800.0, "fallback"
     achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
     tokens_per_s = world * T * steps / (ms / 1e3)
+    roofline = {"bound": "hbm",
+                "kernel": ("decode_fused_kernel (the step's only launch)" if T <= 8
+                           else "whole layer call (all launches of one step)"),
+                "achieved": achieved, "peak": hbm_peak, "peak_source": peak_src,
+                "unit": "GB/s", "frac": achieved / hbm_peak,
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "traffic": NCU_TRAFFIC.get(args.workload)}
+    if stage_ms and T >= 1024:
+        # dense contraction: the up/gate grouped GEMM against the tensor peak
+        # (fp16 operands; GB300's nominal fp16 and bf16 dense rates are equal,
+        # so the measured sustained bf16 cuBLAS rate is the fp16 peak)
+        routes = T * (wl.k + 1)
+        ug_flop = routes * 4.0 * wl.H * wl.F
+        try:
+            tc_peak, tc_src = float(peaks["bf16_tflops_sustained"]), "measured (sustained bf16 = fp16)"
+        except (KeyError, ValueError):
+            tc_peak, tc_src = 1700.0, "fallback"
+        ug_tflops = ug_flop / (stage_ms["up/gate"] * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "grouped_gemm_tc<up/gate>",
+                    "achieved": ug_tflops, "peak": tc_peak, "peak_source": tc_src,
+                    "unit": "TFLOP/s", "frac": ug_tflops / tc_peak,
+                    "algorithmic_flops_per_launch": ug_flop,
+                    "launch_ms": stage_ms["up/gate"], "traffic": NCU_TRAFFIC.get(args.workload)}
     line = {
         "metric": METRIC,
         "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": steps,
@@ -310,11 +372,145 @@ def run_ours(args, rank, world, local_rank):
         "us_per_layer": ms_per_step * 1e3,
         "expert_weight_gbs": expert_bytes / (ms_per_step * 1e-3) / 1e9,
         "expert_weight_frac_of_hbm_peak": expert_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
-        "roofline": {"bound": "hbm", "kernel": "whole layer call (all launches of one step)",
+        "roofline": roofline,
+        "stage_ms": stage_ms,
+        "gpu_launches": gpu_launches,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def run_trunk(args, rank, world, local_rank):
+    """A step is T tokens through the whole trunk: per layer a residual-add +
+    RMSNorm launch and the layer's route + forward launches."""
+    import numpy as np
+    import torch
+    import quantized_moe_expert_sigmoid_gb300 as moe
+    from quantized_moe_expert_sigmoid_gb300 import build as moe_build, synth
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or not os.path.exists(moe_build.LIB):
+        moe_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    wl = synth.WORKLOADS[args.workload]
+    T = wl.T
+    NL, NX, G, cfg = bench_config(args, wl, world)
+    layers, routers = [], []
+    for l in range(NL):
+        ew = synth.expert_weights_torch(1000 * rank + 7, l, wl.E, wl.H, wl.F, device=dev)
+        layers.append(moe.MoeLayer(wl.H, wl.E, wl.k, wl.F, 1, wl.scale, T, up=ew.up, gate=ew.gate,
+                                   down=ew.down, sh_up=ew.sh_up, sh_gate=ew.sh_gate,
+                                   sh_down=ew.sh_down))
+        del ew
+        routers.append(torch.from_numpy(synth.router_weights(7, l, wl.E, wl.H, wl.router_sigma)).to(dev))
+    torch.cuda.empty_cache()
+    trunk = moe.MoeTrunk(layers, routers, T)
+    xs_host = [synth.activations(100 + rank, "trunk", T, wl.H, np.full(T, i)) for i in range(NX)]
+    xs = [torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16) for a in xs_host]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for j in range(max(3, args.warmup)):
+            trunk.forward(xs[j % NX])
+    stream.synchronize()
+    trunk.check()
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(n):
+                trunk.forward(xs[j % NX])
+        return g
+
+    reps, rem = divmod(args.steps, G)
+    launches0 = moe.moe_launch_count()
+    g_main = capture(G) if reps else None
+    launches_per_graph = moe.moe_launch_count() - launches0
+    launches0 = moe.moe_launch_count()
+    g_rem = capture(rem) if rem else None
+    launches_rem = moe.moe_launch_count() - launches0
+    with torch.cuda.stream(stream):
+        for g in (g_main, g_rem):
+            if g:
+                g.replay()
+    stream.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local_rank) as clk:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(reps):
+                g_main.replay()
+            if g_rem:
+                g_rem.replay()
+            stop.record(stream)
+        stop.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = start.elapsed_time(stop)
+    trunk.check()
+    t_ms = torch.tensor([ms], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t_ms, op=torch.distributed.ReduceOp.MAX)
+    ms = float(t_ms.item())
+    steps = reps * G + rem
+    ms_per_step = ms / steps
+    # bytes of the last step: every layer's selected experts + shared, routers, activations
+    distinct = [len(set(trunk.ids[l][:T].flatten().tolist())) for l in range(NL)]
+    expert_bytes = sum(d + 1 for d in distinct) * EXPERT_BYTES
+    alg_bytes = expert_bytes + NL * (wl.E * wl.H * 4 + T * wl.H * (2 + 4 + 4 + 4 + 2))
+
+    e2e = None
+    if rank == 0:
+        n_e2e = max(1, min(args.e2e_steps, args.steps, 200))
+        xh = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in xs_host]
+        rh = torch.empty((T, wl.H), dtype=torch.float32).pin_memory()
+        xd = torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for j in range(4):
+                xd.copy_(xh[j % NX], non_blocking=True)
+                rh.copy_(trunk.forward(xd), non_blocking=True)
+            stream.synchronize()
+            e0.record(stream)
+            for j in range(n_e2e):
+                xd.copy_(xh[j % NX], non_blocking=True)
+                rh.copy_(trunk.forward(xd), non_blocking=True)
+            e1.record(stream)
+        e1.synchronize()
+        e2e = {"value": n_e2e * T / (e0.elapsed_time(e1) / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": T * wl.H * 2, "d2h_bytes_per_step": T * wl.H * 4,
+               "steps": n_e2e}
+    if rank != 0:
+        return
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        hbm_peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        hbm_peak, peak_src = 6800.0, "fallback"
+    achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": world * T * steps / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in, fp32 residual, IQ4_NL weights, fp32 accumulate",
+        "data": "synthetic (seeded; random IQ4_NL weights of the Xing4 trunk shapes)",
+        "config": cfg,
+        "us_per_layer": ms_per_step * 1e3 / NL,
+        "expert_weight_gbs": expert_bytes / (ms_per_step * 1e-3) / 1e9,
+        "expert_weight_frac_of_hbm_peak": expert_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
+        "roofline": {"bound": "hbm", "kernel": f"whole trunk step ({NL} layers, all launches)",
                      "achieved": achieved, "peak": hbm_peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": achieved / hbm_peak,
                      "algorithmic_bytes_per_launch": alg_bytes, "traffic": None},
-        "gpu_launches": gpu_launches,
+        "gpu_launches": reps * launches_per_graph + launches_rem,
         "clocks": clk.summary(),
         "e2e": e2e,
     }
@@ -336,7 +532,10 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
     try:
-        run_ours(args, rank, world, local_rank)
+        if args.workload.startswith("trunk"):
+            run_trunk(args, rank, world, local_rank)
+        else:
+            run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch

@@ -190,6 +190,29 @@ int64_t moe_layer_weight_bytes(moe_layer_t layer);
  * layers, all threads).  Diagnostics: lets a caller count launches per call. */
 int64_t moe_launch_count(void);
 
+/* Stage timing, a profiling aid (the pages have no counterpart).
+ *
+ * moe_layer_enable_timing(layer, calls) makes every later call of
+ * moe_forward / moe_layer_forward_routed on `layer` record five CUDA events
+ * on its stream into the next of `calls` slots (a ring): call start, start
+ * of the up/gate grouped GEMM, its end, end of the down-projection grouped
+ * GEMM, call end.  The single-launch decode path has no separate stages: it
+ * reports its one kernel as the up/gate stage.  The events are recorded with
+ * cudaEventRecordExternal, so inside stream capture they become event-record
+ * nodes and every replay of the graph refreshes them; such an event stays
+ * bound to the graph, so after capturing calls, destroy the graph and call
+ * moe_layer_enable_timing again (0, or a new count: fresh events) before
+ * calling the layer outside it (a reused slot otherwise fails with
+ * MOE_ERR_CUDA).  calls = 0 disables timing and frees the events; calls must
+ * be <= 4096.  Not safe while a call on the layer is in flight.
+ *
+ * moe_layer_stage_times(layer, ms, max_calls, n) synchronises on the events
+ * and writes, for the n (<= max_calls) slots recorded since timing was
+ * enabled (oldest first), four durations in milliseconds: routing + plan +
+ * gather, up/gate, down, combine.  ms holds max_calls * 4 floats (host). */
+moe_status moe_layer_enable_timing(moe_layer_t layer, int32_t calls);
+moe_status moe_layer_stage_times(moe_layer_t layer, float *ms, int32_t max_calls, int32_t *n);
+
 /* Static name of a status code. */
 const char *moe_status_string(moe_status status);
 

@@ -84,8 +84,11 @@ def load_library(path: str | None = None):
     lib.moe_status_string.restype = ctypes.c_char_p
     lib.moe_last_error.argtypes = []
     lib.moe_last_error.restype = ctypes.c_char_p
+    lib.moe_layer_enable_timing.argtypes = [P, I32]
+    lib.moe_layer_stage_times.argtypes = [P, P, I32, ctypes.POINTER(I32)]
     for n in ("moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
-              "moe_layer_forward_routed", "moe_residual_rmsnorm", "moe_layer_check"):
+              "moe_layer_forward_routed", "moe_residual_rmsnorm", "moe_layer_check",
+              "moe_layer_enable_timing", "moe_layer_stage_times"):
         getattr(lib, n).restype = I32
     _lib = lib
     return lib
@@ -232,6 +235,27 @@ def moe_layer_check(layer):
     _check(load_library().moe_layer_check(ctypes.c_void_p(layer)))
 
 
+def moe_layer_enable_timing(layer, calls: int):
+    """Record per-stage CUDA events for the next calls on the layer (a ring of
+    `calls` slots; 0 disables)."""
+    _check(load_library().moe_layer_enable_timing(ctypes.c_void_p(layer), int(calls)))
+
+
+STAGES = ("route+plan+gather", "up/gate", "down", "combine")
+
+
+def moe_layer_stage_times(layer, max_calls: int):
+    """Per-stage milliseconds of the recorded calls, oldest first: a list of
+    4-tuples in the order of STAGES."""
+    import numpy as np
+    ms = np.zeros((max(1, max_calls), 4), np.float32)
+    n = ctypes.c_int32(0)
+    _check(load_library().moe_layer_stage_times(ctypes.c_void_p(layer),
+                                                ms.ctypes.data_as(ctypes.c_void_p),
+                                                int(max_calls), ctypes.byref(n)))
+    return [tuple(float(v) for v in row) for row in ms[:n.value]]
+
+
 def moe_layer_weight_bytes(layer) -> int:
     return int(load_library().moe_layer_weight_bytes(ctypes.c_void_p(layer)))
 
@@ -312,3 +336,47 @@ class MoeLayer:
             self.close()
         except Exception:
             pass
+
+
+class MoeTrunk:
+    """A stack of MoE layers on an fp32 residual stream (the 38-layer trunk
+    of the Xing4.0-29B-A4B model card, MoE blocks only):
+        r_0 = x,  u_l = bf16(r_l / sqrt(mean(r_l^2) + eps)),  r_{l+1} = r_l + MoE_l(u_l).
+    Per layer: one residual-add + RMSNorm launch, then the layer's
+    route + forward launches (layer outputs are fp32, added to r in fp32).
+    Every tensor it uses is preallocated at construction, so forward() can
+    be captured in a CUDA graph."""
+
+    def __init__(self, layers, routers, max_tokens, eps=1e-6, device="cuda"):
+        import torch
+        assert len(layers) == len(routers) and layers
+        self.layers, self.routers, self.eps = list(layers), list(routers), float(eps)
+        H, k = layers[0].H, layers[0].k
+        n = len(layers)
+        self.r = torch.empty((max_tokens, H), dtype=torch.float32, device=device)
+        self.u = [torch.empty((max_tokens, H), dtype=torch.bfloat16, device=device) for _ in range(n)]
+        self.out = [torch.empty((max_tokens, H), dtype=torch.float32, device=device) for _ in range(n)]
+        self.ids = [torch.empty((max_tokens, k), dtype=torch.int32, device=device) for _ in range(n)]
+        self.w = [torch.empty((max_tokens, k), dtype=torch.float32, device=device) for _ in range(n)]
+        self.u_final = torch.empty((max_tokens, H), dtype=torch.bfloat16, device=device)
+
+    def forward(self, x, stream=None):
+        """x: fp32 or bf16 [T, H] on the device.  Returns the final residual
+        r_L [T, H] fp32 (a view of the trunk's buffer); the per-layer u, out,
+        ids and w stay readable in self.u / self.out / self.ids / self.w."""
+        T = x.shape[0]
+        r = self.r[:T]
+        r.copy_(x)
+        prev = None
+        for l, (L, wr) in enumerate(zip(self.layers, self.routers)):
+            u = self.u[l][:T]
+            moe_residual_rmsnorm(r, prev, u, self.eps, stream=stream)
+            out = self.out[l][:T]
+            moe_layer_forward_routed(L.handle, u, wr, self.ids[l][:T], self.w[l][:T], out, stream=stream)
+            prev = out
+        moe_residual_rmsnorm(r, prev, self.u_final[:T], self.eps, stream=stream)  # r_L = r_{L-1} + out
+        return r
+
+    def check(self):
+        for L in self.layers:
+            L.check()

@@ -5,6 +5,7 @@
 // instead of falling back): create validates the shape and allocates every
 // workspace for max_tokens up front; route and forward only validate their
 // arguments (including base-pointer alignment for vector loads) and launch.
+#include <algorithm>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -75,7 +76,24 @@ void free_layer(Layer *L) {
                   L->tiles_ug, L->tiles_dn, L->tile_counts};
   for (void *p : ptrs)
     if (p) cudaFree(p);
+  if (L->tev) {
+    for (int i = 0; i < L->tev_slots * moe::kStageEvents; ++i) cudaEventDestroy(L->tev[i]);
+    delete[] L->tev;
+  }
   delete L;
+}
+
+// The stage-timing events of the call being issued, or nullptr.
+cudaEvent_t *timing_slot(Layer *L) {
+  return L->tev ? L->tev + (size_t)L->tev_next * moe::kStageEvents : nullptr;
+}
+void timing_advance(Layer *L) {
+  if (!L->tev) return;
+  L->tev_next = (L->tev_next + 1) % L->tev_slots;
+  L->tev_used = std::min(L->tev_used + 1, L->tev_slots);
+}
+cudaError_t rec(cudaEvent_t e, cudaStream_t st) {
+  return cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
 }
 
 moe_status check_x(const Layer *L, const void *x, moe_dtype xdt, int32_t T) {
@@ -106,8 +124,11 @@ moe_status route_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const f
   return MOE_OK;
 }
 
+// ev: the call's stage-timing events (nullable); ev[0] was recorded by the
+// caller when start_recorded.
 moe_status forward_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const int32_t *ids,
-                        const float *w, void *out, moe_dtype odt, cudaStream_t st) {
+                        const float *w, void *out, moe_dtype odt, cudaStream_t st,
+                        cudaEvent_t *ev = nullptr, bool start_recorded = false) {
   moe_status s = check_x(L, x, xdt, T);
   if (s != MOE_OK) return s;
   if (odt != MOE_DT_BF16 && odt != MOE_DT_FP32)
@@ -117,16 +138,24 @@ moe_status forward_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const
   if (!moe::aligned(ids, 4) || !moe::aligned(w, 4))
     return fail(MOE_ERR_MISALIGNED, "ids/weights are not 4-byte aligned");
   if (!moe::aligned(out, 16)) return fail(MOE_ERR_MISALIGNED, "out is not 16-byte aligned");
+  if (ev && !start_recorded) MOE_CUDA(rec(ev[0], st), "timing event");
   if (moe::fused_decode_supported(*L, T)) {
+    if (ev) MOE_CUDA(rec(ev[1], st), "timing event");
     MOE_CUDA(moe::launch_decode_fused(*L, x, xdt, T, nullptr, nullptr, 0, ids, w, nullptr, nullptr,
                                       out, odt, st),
              "fused decode");
+    if (ev) {
+      MOE_CUDA(rec(ev[2], st), "timing event");
+      MOE_CUDA(rec(ev[3], st), "timing event");
+      MOE_CUDA(rec(ev[4], st), "timing event");
+    }
     return MOE_OK;
   }
   MOE_CUDA(cudaMemsetAsync(L->out_acc, 0, sizeof(float) * (size_t)T * L->H, st), "clear accumulator");
   MOE_CUDA(moe::launch_route_plan(*L, ids, w, T, st), "route plan");
-  MOE_CUDA(moe::launch_prefill_tc(*L, x, xdt, T, st), "tensor-core expert GEMMs");
+  MOE_CUDA(moe::launch_prefill_tc(*L, x, xdt, T, st, ev ? ev + 1 : nullptr), "tensor-core expert GEMMs");
   MOE_CUDA(moe::launch_finalize(*L, T, out, odt, st), "finalize");
+  if (ev) MOE_CUDA(rec(ev[4], st), "timing event");
   return MOE_OK;
 }
 
@@ -264,8 +293,11 @@ moe_status moe_route(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_
 moe_status moe_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
                        const int32_t *ids, const float *weights, void *out, moe_dtype out_dtype,
                        void *stream) {
-  return forward_impl(reinterpret_cast<Layer *>(layer), x, x_dtype, T, ids, weights, out,
-                      out_dtype, (cudaStream_t)stream);
+  Layer *L = reinterpret_cast<Layer *>(layer);
+  cudaEvent_t *ev = (L && T > 0) ? timing_slot(L) : nullptr;
+  moe_status r = forward_impl(L, x, x_dtype, T, ids, weights, out, out_dtype, (cudaStream_t)stream, ev);
+  if (r == MOE_OK && ev) timing_advance(L);
+  return r;
 }
 
 moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype x_dtype,
@@ -286,14 +318,29 @@ moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype 
     if (!moe::aligned(ids, 4) || !moe::aligned(weights, 4))
       return fail(MOE_ERR_MISALIGNED, "ids/weights are not 4-byte aligned");
     if (logit_bias && bias_row_stride < 0) return fail(MOE_ERR_INVALID_ARG, "bias_row_stride is negative");
+    cudaEvent_t *ev = timing_slot(L);
+    if (ev) {
+      MOE_CUDA(rec(ev[0], st), "timing event");
+      MOE_CUDA(rec(ev[1], st), "timing event");
+    }
     MOE_CUDA(moe::launch_decode_fused(*L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, nullptr,
                                       nullptr, ids, weights, out, out_dtype, st),
              "fused decode");
+    if (ev) {
+      MOE_CUDA(rec(ev[2], st), "timing event");
+      MOE_CUDA(rec(ev[3], st), "timing event");
+      MOE_CUDA(rec(ev[4], st), "timing event");
+      timing_advance(L);
+    }
     return MOE_OK;
   }
+  cudaEvent_t *ev = (L && T > 0) ? timing_slot(L) : nullptr;
+  if (ev) MOE_CUDA(rec(ev[0], st), "timing event");
   moe_status s = route_impl(L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, ids, weights, st);
   if (s != MOE_OK) return s;
-  return forward_impl(L, x, x_dtype, T, ids, weights, out, out_dtype, st);
+  s = forward_impl(L, x, x_dtype, T, ids, weights, out, out_dtype, st, ev, true);
+  if (s == MOE_OK && ev) timing_advance(L);
+  return s;
 }
 
 moe_status moe_residual_rmsnorm(float *resid, const void *delta, moe_dtype delta_dtype, void *u,
@@ -308,6 +355,48 @@ moe_status moe_residual_rmsnorm(float *resid, const void *delta, moe_dtype delta
     return fail(MOE_ERR_MISALIGNED, "resid, delta and u must be 16-byte aligned");
   MOE_CUDA(moe::launch_residual_rmsnorm(resid, delta, delta_dtype, u, T, H, eps, (cudaStream_t)stream),
            "residual rmsnorm");
+  return MOE_OK;
+}
+
+moe_status moe_layer_enable_timing(moe_layer_t layer, int32_t calls) {
+  Layer *L = reinterpret_cast<Layer *>(layer);
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+  if (calls < 0 || calls > 4096) return fail(MOE_ERR_INVALID_ARG, "calls = %d: need 0..4096", calls);
+  if (L->tev) {
+    for (int i = 0; i < L->tev_slots * moe::kStageEvents; ++i) cudaEventDestroy(L->tev[i]);
+    delete[] L->tev;
+    L->tev = nullptr;
+  }
+  L->tev_slots = L->tev_next = L->tev_used = 0;
+  if (calls == 0) return MOE_OK;
+  const int n = calls * moe::kStageEvents;
+  cudaEvent_t *ev = new cudaEvent_t[n];
+  for (int i = 0; i < n; ++i) {
+    const cudaError_t e = cudaEventCreate(&ev[i]);
+    if (e != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+      delete[] ev;
+      return cuda_fail(e, "cudaEventCreate");
+    }
+  }
+  L->tev = ev;
+  L->tev_slots = calls;
+  return MOE_OK;
+}
+
+moe_status moe_layer_stage_times(moe_layer_t layer, float *ms, int32_t max_calls, int32_t *n) {
+  Layer *L = reinterpret_cast<Layer *>(layer);
+  if (!L || !n || (max_calls > 0 && !ms) || max_calls < 0)
+    return fail(MOE_ERR_INVALID_ARG, "layer, n and ms must be non-NULL, max_calls >= 0");
+  const int used = std::min(L->tev_used, (int)max_calls);
+  const int first = (L->tev_next - L->tev_used + L->tev_slots) % std::max(L->tev_slots, 1);
+  for (int i = 0; i < used; ++i) {
+    const cudaEvent_t *ev = L->tev + (size_t)((first + i) % L->tev_slots) * moe::kStageEvents;
+    MOE_CUDA(cudaEventSynchronize(ev[moe::kStageEvents - 1]), "timing event");
+    for (int k = 0; k + 1 < moe::kStageEvents; ++k)
+      MOE_CUDA(cudaEventElapsedTime(&ms[(size_t)i * 4 + k], ev[k], ev[k + 1]), "timing event");
+  }
+  *n = used;
   return MOE_OK;
 }
 

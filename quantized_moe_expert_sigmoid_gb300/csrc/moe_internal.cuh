@@ -38,6 +38,7 @@ constexpr int kFusedMaxTokens = 8;
 // Sticky device error bits (Layer::err).
 constexpr unsigned kErrBadId = 1u;
 constexpr unsigned kErrTimeout = 2u;
+constexpr int kStageEvents = 5;  // call start, up/gate begin, up/gate end, down end, call end
 constexpr unsigned kErrOverflow = 4u;  // a value left fp16 range on the tensor-core path
 
 // One tile of the batched tensor-core path: expert id, weight tile (128
@@ -80,6 +81,9 @@ struct Layer {
   __half *h16 = nullptr;     // [max_routes][Fp] SwiGLU outputs, fp16
   TcTile *tiles_ug = nullptr, *tiles_dn = nullptr;
   int *tile_counts = nullptr;  // [2]
+  // opt-in stage timing: kStageEvents events per call slot (see the header)
+  cudaEvent_t *tev = nullptr;
+  int tev_slots = 0, tev_next = 0, tev_used = 0;
   CUtensorMap map_x16, map_h16;        // activation tiles of the tensor-core path
   CUtensorMap map_gu_lab, map_dn_lab;  // weight labels of one k-step
 };
@@ -136,7 +140,9 @@ cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, in
 // prefill_tc.cu: grouped GEMMs on tcgen05 for T > kFusedMaxTokens.
 int tc_max_tiles(const Layer &L, bool up_gate);
 cudaError_t tc_prepare(Layer &L);  // tensor maps + kernel attributes (after workspace allocation)
-cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int T, cudaStream_t stream);
+// ev: nullable; the events to record before up/gate, after up/gate and after down
+cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int T, cudaStream_t stream,
+                              cudaEvent_t *ev = nullptr);
 
 // norm.cu
 cudaError_t launch_residual_rmsnorm(float *resid, const void *delta, moe_dtype ddt,

@@ -598,7 +598,7 @@ cudaError_t tc_prepare(Layer &L) {
 }
 
 cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int T,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, cudaEvent_t *ev) {
   const int max_rows = T * L.k + L.S * T;
   // tile lists
   build_tiles_kernel<<<1, kTileThreads, 0, stream>>>(L.offsets, L.active, L.E + L.S, L.Fp / kTM,
@@ -635,9 +635,11 @@ cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int 
   p.w = L.gu;
   p.row_bytes = L.gu_row_bytes;
   p.rows_per_expert = 2 * (int64_t)L.Fp;
+  if (ev && (e = cudaEventRecordWithFlags(ev[0], stream, cudaEventRecordExternal)) != cudaSuccess) return e;
   grouped_gemm_tc<true><<<g_sms_tc, kThreadsTC, tc_smem(), stream>>>(p, L.map_x16, L.map_gu_lab);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (ev && (e = cudaEventRecordWithFlags(ev[1], stream, cudaEventRecordExternal)) != cudaSuccess) return e;
   // down + weighted scatter
   p.tiles = L.tiles_dn;
   p.n_tiles = L.tile_counts + 1;
@@ -646,7 +648,9 @@ cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int 
   p.rows_per_expert = L.Hp;
   grouped_gemm_tc<false><<<g_sms_tc, kThreadsTC, tc_smem(), stream>>>(p, L.map_h16, L.map_dn_lab);
   count_launches(1);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (ev) return cudaEventRecordWithFlags(ev[2], stream, cudaEventRecordExternal);
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -152,6 +152,26 @@ def expert_weights(seed: int, layer: int, E: int, H: int, F: int,
     return ExpertWeights(up, gate, down, s_up, s_gate, s_down)
 
 
+def expert_subset_weights(seed: int, layer: int, experts, H: int, F: int,
+                          n_shared: int = 1) -> ExpertWeights:
+    """The matrices of the routed experts `experts` (in that order) of layer
+    `layer`, plus the shared expert: the same bytes as expert_weights(...)
+    for those experts, without drawing the others."""
+    ids = [int(e) for e in experts]
+    up = np.stack([iq4nl_blocks(seed, "up", F, H, layer, e) for e in ids])
+    gate = np.stack([iq4nl_blocks(seed, "gate", F, H, layer, e) for e in ids])
+    down = np.stack([iq4nl_blocks(seed, "down", H, F, layer, e) for e in ids])
+    if n_shared:
+        s_up = iq4nl_blocks(seed, "sh_up", F, H, layer)
+        s_gate = iq4nl_blocks(seed, "sh_gate", F, H, layer)
+        s_down = iq4nl_blocks(seed, "sh_down", H, F, layer)
+    else:
+        s_up = np.zeros((F, H // QK, BLOCK_BYTES), np.uint8)
+        s_gate = np.zeros_like(s_up)
+        s_down = np.zeros((H, F // QK, BLOCK_BYTES), np.uint8)
+    return ExpertWeights(up, gate, down, s_up, s_gate, s_down)
+
+
 # --------------------------------------------------------------------------
 # Activations, router weights, logit bias
 # --------------------------------------------------------------------------

@@ -90,3 +90,10 @@ def test_rmsnorm_argument_checks(lib):
     assert lib.moe_residual_rmsnorm(None, None, 1, None, 1, 16, 1e-6, None) == 1   # NULL
     assert lib.moe_residual_rmsnorm(ctypes.c_void_p(8), None, 1, ctypes.c_void_p(16), 1, 16,
                                     1e-6, None) == 3                                # misaligned
+
+
+def test_stage_timing_argument_checks(lib):
+    assert lib.moe_layer_enable_timing(None, 4) == 1      # NULL layer
+    n = ctypes.c_int32(-1)
+    assert lib.moe_layer_stage_times(None, None, 0, ctypes.byref(n)) == 1
+    assert moe.STAGES == ("route+plan+gather", "up/gate", "down", "combine")
