@@ -119,8 +119,15 @@ moe_status route_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const f
   if (!moe::aligned(ids, 4) || !moe::aligned(w, 4))
     return fail(MOE_ERR_MISALIGNED, "ids/weights are not 4-byte aligned");
   if (bias && bstride < 0) return fail(MOE_ERR_INVALID_ARG, "bias_row_stride is negative");
-  MOE_CUDA(moe::launch_router_logits(*L, x, xdt, T, wr, bias, bstride, L->logits, st), "router logits");
-  MOE_CUDA(moe::launch_router_topk(*L, L->logits, T, ids, w, st), "router top-k");
+  int parts;
+  if (moe::router_tc_supported(*L, xdt, T)) {  // large bf16 batches: tensor cores
+    parts = moe::router_tc_parts(*L, T);
+    MOE_CUDA(moe::launch_router_tc(*L, x, T, wr, L->logits, parts, st), "router logits");
+  } else {
+    parts = moe::router_parts(T, moe::kRouterMaxParts);
+    MOE_CUDA(moe::launch_router_logits(*L, x, xdt, T, wr, L->logits, parts, st), "router logits");
+  }
+  MOE_CUDA(moe::launch_router_topk(*L, L->logits, parts, bias, bstride, T, ids, w, st), "router top-k");
   return MOE_OK;
 }
 
@@ -229,7 +236,7 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   const int64_t dn_total = (int64_t)(E + S) * L->dn_expert_bytes;
   ALLOC(L->gu, gu_total);
   ALLOC(L->dn, dn_total);
-  ALLOC(L->logits, sizeof(float) * (int64_t)sh->max_tokens * E);
+  ALLOC(L->logits, sizeof(float) * (int64_t)moe::kRouterMaxParts * sh->max_tokens * E);
   ALLOC(L->offsets, sizeof(int) * (E + S + 1));
   ALLOC(L->active, sizeof(int) * (E + S + 1));
   ALLOC(L->route_token, sizeof(int) * (int64_t)L->max_routes);

@@ -191,9 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     };
     int issued = 0;
     if (lane == 0) {
-      for (; issued < n_shared_items && issued < nst; ++issued) issue(issued);
-      if (S && nrows > 0)  // the shared expert's W_down rows of this CTA, known before routing
-        bulk_prefetch_l2(L.dn + (int64_t)E * L.dn_expert_bytes + (int64_t)n0 * db, (uint32_t)(nrows * db));
+      // the router rows first (the routing is on the critical path), then
+      // the shared expert's rows, known before routing
       if (do_route && p.wr_rows_smem > 0) {  // router rows -> last stage (no shared item uses it)
         int nr = 0;
         for (int e = c; e < E; e += G) ++nr;
@@ -205,6 +204,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
                      (uint32_t)(H * 4), &wr_bar);
         }
       }
+      // a router CTA lets its router row land first: HBM is busy with every
+      // CTA's shared-expert rows at this point, and the routing is what the
+      // whole grid waits for
+      if (do_route && p.wr_rows_smem > 0 && c < E && !mbar_wait_bounded(&wr_bar, 0, kPollLimit))
+        atomicOr(&status, 2);
+      for (; issued < n_shared_items && issued < nst; ++issued) issue(issued);
+      if (S && nrows > 0)  // the shared expert's W_down rows of this CTA
+        bulk_prefetch_l2(L.dn + (int64_t)E * L.dn_expert_bytes + (int64_t)n0 * db, (uint32_t)(nrows * db));
     }
     if (do_route && p.wr_rows_smem == 0)
       for (int e = c; e < E; e += G)
@@ -238,14 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
 #pragma unroll
           for (int i = 0; i < 8; ++i) key[i] = lane + 32 * i < E ? float_order_key(v[i]) : 0u;
           unsigned taken = 0;
-          float ssum = 0.f, my_s = 0.f;
+          uint32_t my_key = 0;
           int my_id = 0;
+          const int nloc = (E + 31) >> 5;  // logits per lane
           for (int j = 0; j < K; ++j) {
             uint32_t lk = 0;
             int li = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              if (!((taken >> i) & 1u) && key[i] > lk) {
+              if (i < nloc && !((taken >> i) & 1u) && key[i] > lk) {
                 lk = key[i];
                 li = i;
               }
@@ -253,13 +261,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             const int bid =
                 (int)__reduce_min_sync(0xffffffffu, lk == m ? (uint32_t)(lane + 32 * li) : 0xffffffffu);
             if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-            const float sg = 1.0f / (1.0f + expf(-float_from_order_key(m)));
-            ssum += sg;
             if (lane == j) {
               my_id = bid;
-              my_s = sg;
+              my_key = m;
             }
           }
+          // the k scores in parallel, lane j holding the j-th
+          const float my_s = lane < K ? 1.0f / (1.0f + expf(-float_from_order_key(my_key))) : 0.f;
+          const float ssum = warp_sum(my_s);
           if (lane < K) {
             const float wgt = L.scale * my_s / ssum;
             sel_id[t][lane] = my_id;
@@ -336,7 +345,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         n_ex = nex;
         ex_rs[nex] = sb0 + n_valid;
       }
-      __syncwarp();
+      __syncwarp();  // ex_id / ex_rs / n_ex of every lane
+      if (lane == 0) {
+        // The items come first, counted in a register: this CTA's share of
+        // the routed up/gate rows, then its W_down rows.  Their loads go out
+        // at once, before the rest of the plan.
+        int ni = n_items;
+        const int D = nex - S;
+        const int64_t N = (int64_t)D * Fp;
+        const int64_t fb = (int64_t)c * N / G, fe = (int64_t)(c + 1) * N / G;
+        for (int a = S; a < nex; ++a) {
+          const int64_t lo = (int64_t)(a - S) * Fp, hi = lo + Fp;
+          int f = (int)(max(fb, lo) - lo);
+          const int f_end = (int)(min(fe, hi) - lo);
+          while (f < f_end && ni < kMaxItems) {
+            const int grp_end = (f / kGroupRows + 1) * kGroupRows;
+            const int cnt = min(min(f_end, grp_end) - f, p.fpi);
+            items[ni++] = Item{0, (int16_t)a, f, cnt};
+            f += cnt;
+          }
+        }
+        for (int a = 0; a < nex && ni < kMaxItems; ++a) items[ni++] = Item{1, (int16_t)a, n0, nrows};
+        n_items = ni;
+        if (issued < ni && issued < nst) issue(issued++);  // the first routed rows at once
+      }
       for (int idx = lane; idx < (nex - S) * T; idx += 32) {  // route of token t in expert a
         const int a = S + idx / T, t = idx % T;
         int r = -1;
@@ -344,29 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           if (r_tok[sl] == t) r = sl - ex_rs[a];
         rid[a][t] = (int8_t)r;
       }
-      if (lane == 0) {  // this CTA's share of the routed up/gate rows, then its W_down rows
-        const int D = nex - S;
-        const int64_t N = (int64_t)D * Fp;
-        const int64_t fb = (int64_t)c * N / G, fe = (int64_t)(c + 1) * N / G;
-        for (int a = S; a < nex; ++a) {
-          const int64_t lo = (int64_t)(a - S) * Fp, hi = lo + Fp;
-          const int64_t q0 = max(fb, lo), q1 = min(fe, hi);
-          if (q0 < q1) add_upgate(a, (int)(q0 - lo), (int)(q1 - lo));
-        }
-        for (int a = 0; a < nex && n_items < kMaxItems; ++a)
-          items[n_items++] = Item{1, (int16_t)a, n0, nrows};
-      }
     }
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(&plan_bar);  // release: the tables above become visible to the waiters
       int i = issued;
       for (; i < n_items && i < nst; ++i) issue(i);  // stages never used yet
-      // this CTA's W_down rows of every routed expert into L2 now: their
-      // ring stages free up only as the up/gate items are consumed
-      for (int a = S; a < n_ex && nrows > 0; ++a)
-        bulk_prefetch_l2(L.dn + (int64_t)ex_id[a] * L.dn_expert_bytes + (int64_t)n0 * db,
-                         (uint32_t)(nrows * db));
       for (; i < n_items; ++i) {
         const int s = i % nst;
         if (!mbar_wait_bounded(&empty_bar[s], (uint32_t)((i / nst) - 1) & 1u, kPollLimit)) {
@@ -429,18 +444,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           if (lane == 0) red[warp][t] = v;
         }
         named_sync(kBarConsumers, kConsumers);
-        if (ct < T) {
-          float v = 0.f;
-          for (int w2 = 0; w2 < kConsumerWarps; ++w2) v += red[w2][ct];
-          if (p.bias) v += p.bias[(int64_t)ct * p.bstride + e];
-          L.logits[(int64_t)ct * E + e] = v;
+        if (warp == 0) {  // the 16 warp partials of each token, one more warp sum
+          for (int t = 0; t < T; ++t) {
+            float v = warp_sum(lane < kConsumerWarps ? red[lane][t] : 0.f);
+            if (lane == 0) {
+              if (p.bias) v += p.bias[(int64_t)t * p.bstride + e];
+              L.logits[(int64_t)t * E + e] = v;
+            }
+          }
         }
-        named_sync(kBarConsumers, kConsumers);
+        named_sync(kBarConsumers, kConsumers);  // `red` is reused by the next expert
       }
-      if (ct == 0) {
-        __threadfence();
-        atomicAdd(&p.sync[0], 1u);
-      }
+      // this CTA's logits were all written by thread 0: a release add
+      // publishes them (the producers read them after an acquire)
+      if (ct == 0) red_release_add(&p.sync[0], 1u);
     }
     named_sync(kBarConsumers, kConsumers);  // router done with the raw x
 
@@ -593,8 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
       // ---- every CTA's h written ----
       named_sync(kBarConsumers, kConsumers);
       if (ct == 0) {
-        __threadfence();
-        atomicAdd(&p.sync[1], 1u);
+        red_release_add(&p.sync[1], 1u);  // every consumer's h, ordered by the barrier above
         if (!spin_until_geq(&p.sync[1], (unsigned)G, kSpinLimit)) {
           atomicOr(&status, 1);
           atomicOr(L.err, kErrTimeout);

@@ -110,11 +110,16 @@ cudaError_t launch_repack(const uint8_t *src, int rows, int K, uint8_t *dst,
                           int row_group_offset, cudaStream_t stream);
 
 // router.cu
+// Large batches split H into parts whose partial logits are summed by the
+// top-k kernel in part order; `logits` holds parts * T * E floats.
+constexpr int kRouterMaxParts = 8;
+int router_parts(int T, int max_parts);
 cudaError_t launch_router_logits(const Layer &L, const void *x, moe_dtype xdt, int T,
-                                 const float *wr, const float *bias, int64_t bias_stride,
-                                 float *logits, cudaStream_t stream);
-cudaError_t launch_router_topk(const Layer &L, const float *logits, int T, int32_t *ids,
-                               float *weights, cudaStream_t stream);
+                                 const float *wr, float *logits, int parts, cudaStream_t stream);
+// sums the parts, adds the optional bias, selects; ids/weights [T][k]
+cudaError_t launch_router_topk(const Layer &L, const float *logits, int parts, const float *bias,
+                               int64_t bias_stride, int T, int32_t *ids, float *weights,
+                               cudaStream_t stream);
 
 // plan.cu: histogram, prefix sum and stable permutation of the routes.
 cudaError_t launch_route_plan(const Layer &L, const int32_t *ids, const float *weights,
@@ -136,6 +141,18 @@ cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, in
                                 const float *wr, const float *bias, int64_t bstride,
                                 const int32_t *ids_in, const float *w_in, int32_t *ids_out,
                                 float *w_out, void *out, moe_dtype odt, cudaStream_t stream);
+
+// prefill_tc.cu: 2D tensor-map encoding (driver entry point resolved once).
+cudaError_t encode_2d(CUtensorMap *map, CUtensorMapDataType dt, void *base, uint64_t inner,
+                      uint64_t rows, uint64_t row_pitch, uint32_t box_inner, uint32_t box_rows,
+                      CUtensorMapSwizzle swz);
+
+// router_tc.cu: router logits of large bf16 batches on tcgen05 (K-partial
+// sums in the same layout as launch_router_logits).  false: not applicable.
+bool router_tc_supported(const Layer &L, moe_dtype xdt, int T);
+int router_tc_parts(const Layer &L, int T);
+cudaError_t launch_router_tc(const Layer &L, const void *x, int T, const float *wr, float *logits,
+                             int parts, cudaStream_t stream);
 
 // prefill_tc.cu: grouped GEMMs on tcgen05 for T > kFusedMaxTokens.
 int tc_max_tiles(const Layer &L, bool up_gate);

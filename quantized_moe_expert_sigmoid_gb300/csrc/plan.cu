@@ -11,23 +11,48 @@
 //
 // One CTA of 1024 threads (32 warps).  Warp w owns a contiguous run of
 // routes and walks it 32 at a time: lanes with the same expert find each
-// other with __match_any_sync, and a lane's rank is the number of equal
-// lanes below it, so per-(warp, expert) counts and ranks are exact and in
+// other by ballots on the bits of the id, and a lane's rank is the number of
+// equal lanes below it, so per-(warp, expert) counts and ranks are exact and in
 // order.  Pass 1 counts, a scan turns counts into bases in expert-major,
-// warp-minor order, pass 2 writes each route at base + rank.
+// warp-minor order, pass 2 writes each route at base + rank.  Each lane
+// loads 16 routes per round at once, so a pass costs one load round trip
+// per 16,384 routes.  The same CTA then writes the tile lists of the
+// tensor-core path (route tiles of <= 256 per expert, every weight tile of
+// each), from the offsets it holds in shared memory.
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kMaxE = 256;
+constexpr int kPerLane = 16;
+
+// Lanes of the warp holding the same expert id as this lane (ids < 256; ok =
+// false joins no group): one ballot for validity and one per id bit, every
+// lane voting in every ballot.
+__device__ __forceinline__ unsigned same_expert_lanes(int e, bool ok) {
+  unsigned peers = __ballot_sync(0xffffffffu, ok);
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const bool bit = (e >> b) & 1;
+    const unsigned m = __ballot_sync(0xffffffffu, bit);
+    peers &= bit ? m : ~m;
+  }
+  return ok ? peers : 0u;
+}  // routes a lane holds per round (one load round trip)
+constexpr int kTileRoutes = 256;
 
 __global__ void __launch_bounds__(1024) route_plan_kernel(
     const int32_t *__restrict__ ids, const float *__restrict__ wts, int T, int k, int E, int S,
     int *__restrict__ offsets, int *__restrict__ active, int *__restrict__ route_token,
-    float *__restrict__ route_weight, unsigned *__restrict__ err) {
+    float *__restrict__ route_weight, unsigned *__restrict__ err, TcTile *__restrict__ ug,
+    TcTile *__restrict__ dn, int *__restrict__ tile_counts, int ug_mtiles, int dn_mtiles, int max_ug,
+    int max_dn) {
   __shared__ int cnt[32 * kMaxE];  // [warp][expert] counts, then bases
   __shared__ int off[kMaxE + 2];
+  __shared__ int act[kMaxE + 2];
+  __shared__ int tile_base[kMaxE + 2];
+  __shared__ int n_act_s, n_rt_s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int R = T * k;
   const int chunk = ((R + 31) / 32 + 31) & ~31;  // routes per warp, multiple of 32
@@ -38,16 +63,24 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(
   for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
 
-  // pass 1: counts
-  for (int base = r_beg; base < r_end; base += 32) {
-    const int r = base + lane;
-    const bool valid = r < r_end;
-    const int e = valid ? ids[r] : -1;
-    const bool ok = valid && e >= 0 && e < E;
-    if (valid && !ok) atomicOr(err, kErrBadId);
-    const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1);
-    if (ok && (peers & lt_mask) == 0) cnt[warp * E + e] += __popc(peers);
-    __syncwarp();
+  // pass 1: counts (a round = 32 * kPerLane routes of the warp, loaded at once)
+  for (int base = r_beg; base < r_end; base += 32 * kPerLane) {
+    int ev[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+      const int r = base + 32 * i + lane;
+      ev[i] = r < r_end ? ids[r] : -2;
+    }
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+      if (base + 32 * i >= r_end) break;  // warp-uniform
+      const int e = ev[i];
+      const bool ok = e >= 0 && e < E;
+      if (e != -2 && !ok) atomicOr(err, kErrBadId);
+      const unsigned peers = same_expert_lanes(e, ok);
+      if (ok && (peers & lt_mask) == 0) cnt[warp * E + e] += __popc(peers);
+      __syncwarp();
+    }
   }
   __syncthreads();
 
@@ -62,45 +95,107 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(
     off[tid] = run;  // total of expert tid, turned into its start below
   }
   __syncthreads();
-  if (tid == 0) {
-    int run = 0, n_act = 0;
-    for (int e = 0; e < E; ++e) {
-      const int c = off[e];
-      off[e] = run;
-      offsets[e] = run;
-      if (c > 0) active[n_act++] = e;
-      run += c;
+  if (warp == 0) {  // expert starts, active list and route-tile bases, 32 experts at a time
+    int run = 0, n_act = 0, nrt = 0;
+    for (int e0 = 0; e0 < E + S; e0 += 32) {
+      const int e = e0 + lane;
+      int c = 0;
+      if (e < E) c = off[e];
+      else if (e == E && S) c = T;  // the shared expert's segment
+      const bool in = e < E + S;
+      // inclusive scans of the counts and of the route-tile counts
+      const int ntile = (c + kTileRoutes - 1) / kTileRoutes;
+      int cs = c, ts = ntile;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, cs, d), b2 = __shfl_up_sync(0xffffffffu, ts, d);
+        if (lane >= d) {
+          cs += a;
+          ts += b2;
+        }
+      }
+      const unsigned act_mask = __ballot_sync(0xffffffffu, in && c > 0);
+      const int slot = n_act + __popc(act_mask & ((1u << lane) - 1u));
+      if (in) {
+        off[e] = run + cs - c;
+        offsets[e] = run + cs - c;
+        if (c > 0) {
+          act[slot] = e;
+          active[slot] = e;
+          tile_base[slot] = nrt + ts - ntile;
+        }
+      }
+      run += __shfl_sync(0xffffffffu, cs, 31);
+      nrt += __shfl_sync(0xffffffffu, ts, 31);
+      n_act += __popc(act_mask);
     }
-    off[E] = run;
-    offsets[E] = run;
-    if (S) {
-      offsets[E + 1] = run + T;
-      if (T > 0) active[n_act++] = E;
+    if (lane == 0) {
+      off[E + S] = run;
+      offsets[E + S] = run;
+      active[E + S] = n_act;
+      n_act_s = n_act;
+      n_rt_s = nrt;
     }
-    active[E + S] = n_act;
   }
   __syncthreads();
 
   // pass 2: scatter
-  for (int base = r_beg; base < r_end; base += 32) {
-    const int r = base + lane;
-    const bool valid = r < r_end;
-    const int e = valid ? ids[r] : -1;
-    const bool ok = valid && e >= 0 && e < E;
-    const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1);
-    if (ok) {
-      const int pos = off[e] + cnt[warp * E + e] + __popc(peers & lt_mask);
-      route_token[pos] = r / k;
-      route_weight[pos] = wts[r];
+  for (int base = r_beg; base < r_end; base += 32 * kPerLane) {
+    int ev[kPerLane];
+    float wv[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+      const int r = base + 32 * i + lane;
+      ev[i] = r < r_end ? ids[r] : -1;
+      wv[i] = r < r_end ? wts[r] : 0.f;
     }
-    __syncwarp();
-    if (ok && (peers & lt_mask) == 0) cnt[warp * E + e] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+      if (base + 32 * i >= r_end) break;  // warp-uniform
+      const int r = base + 32 * i + lane;
+      const int e = ev[i];
+      const bool ok = e >= 0 && e < E;
+      const unsigned peers = same_expert_lanes(e, ok);
+      if (ok) {
+        const int pos = off[e] + cnt[warp * E + e] + __popc(peers & lt_mask);
+        route_token[pos] = r / k;
+        route_weight[pos] = wv[i];
+      }
+      __syncwarp();
+      if (ok && (peers & lt_mask) == 0) cnt[warp * E + e] += __popc(peers);
+      __syncwarp();
+    }
   }
   if (S) {
     for (int t = tid; t < T; t += blockDim.x) {
       route_token[off[E] + t] = t;
       route_weight[off[E] + t] = 1.0f;
+    }
+  }
+
+  // tile lists of the tensor-core path: per active expert, route tiles of
+  // <= 256 and per route tile every weight tile, in the active order
+  if (ug) {
+    const int n_act = n_act_s;
+    for (int i = tid; i < n_act; i += blockDim.x) {
+      const int e = act[i];
+      const int beg = off[e], cntr = off[e + 1] - beg;
+      const int nrt = (cntr + kTileRoutes - 1) / kTileRoutes;
+      for (int j = 0; j < nrt; ++j) {
+        const int c = min(kTileRoutes, cntr - j * kTileRoutes);
+        for (int m = 0; m < ug_mtiles; ++m) {
+          const int idx = (tile_base[i] + j) * ug_mtiles + m;
+          if (idx < max_ug) ug[idx] = TcTile{e, m, beg + j * kTileRoutes, c};
+        }
+        for (int m = 0; m < dn_mtiles; ++m) {
+          const int idx = (tile_base[i] + j) * dn_mtiles + m;
+          if (idx < max_dn) dn[idx] = TcTile{e, m, beg + j * kTileRoutes, c};
+        }
+      }
+    }
+    if (tid == 0) {
+      tile_counts[0] = min(n_rt_s * ug_mtiles, max_ug);
+      tile_counts[1] = min(n_rt_s * dn_mtiles, max_dn);
     }
   }
 }
@@ -110,7 +205,9 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(
 cudaError_t launch_route_plan(const Layer &L, const int32_t *ids, const float *weights, int T,
                               cudaStream_t stream) {
   route_plan_kernel<<<1, 1024, 0, stream>>>(ids, weights, T, L.k, L.E, L.S, L.offsets, L.active,
-                                            L.route_token, L.route_weight, L.err);
+                                            L.route_token, L.route_weight, L.err, L.tiles_ug,
+                                            L.tiles_dn, L.tile_counts, L.Fp / 128, L.Hp / 256,
+                                            tc_max_tiles(L, true), tc_max_tiles(L, false));
   count_launches(1);
   return cudaGetLastError();
 }

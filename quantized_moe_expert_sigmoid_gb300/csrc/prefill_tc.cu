@@ -39,6 +39,7 @@
 
 #include "device_utils.cuh"
 #include "moe_internal.cuh"
+#include "tc_utils.cuh"
 
 namespace moe {
 namespace {
@@ -85,46 +86,6 @@ __device__ __forceinline__ void codes_to_half(uint32_t c, __half2 d2, uint32_t &
   hi = *reinterpret_cast<uint32_t *>(&hb);
 }
 
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
-  d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: 8 rows x 128 B
-  d |= (uint64_t)1 << 46;            // descriptor version
-  d |= (uint64_t)2 << 61;            // 128-byte swizzle
-  return d;
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1,
-                                            uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_f16(uint32_t tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_addr(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
 struct TcParams {
   const TcTile *tiles;
   const int *n_tiles;
@@ -159,17 +120,6 @@ __device__ __forceinline__ int tile_row(int m, int r) {
   }
   return kRowsTile * m + r;
 }
-
-__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
-      " [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // UG = true: up/gate + SwiGLU epilogue; UG = false: down + weighted scatter.
 template <bool UG>
@@ -425,62 +375,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   if (tid == 0 && abort_flag) atomicOr(p.err, kErrTimeout);
 }
 
-// Tile lists from the route plan: for every expert with routes, route tiles
-// of <= 256 and, per route tile, every weight tile (Fp/128 up/gate tiles,
-// Hp/256 down tiles), expert by expert in the order of the active list.
-// One block: thread i counts the route tiles of active expert i, a block
-// scan places them, and each thread writes its own expert's tiles.
-constexpr int kTileThreads = 256;
-__global__ void __launch_bounds__(kTileThreads)
-    build_tiles_kernel(const int *offsets, const int *active, int n_slots_idx, int ug_mtiles,
-                       int dn_mtiles, TcTile *ug, TcTile *dn, int *counts, int max_ug, int max_dn) {
-  __shared__ int warp_sum[kTileThreads / 32];
-  __shared__ int carry;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int n_act = active[n_slots_idx];
-  if (tid == 0) carry = 0;
-  __syncthreads();
-  for (int i0 = 0; i0 < n_act; i0 += kTileThreads) {
-    const int i = i0 + tid;
-    int e = 0, beg = 0, cnt = 0, nrt = 0;
-    if (i < n_act) {
-      e = active[i];
-      beg = offsets[e];
-      cnt = offsets[e + 1] - beg;
-      nrt = (cnt + kNT - 1) / kNT;
-    }
-    int incl = nrt;  // inclusive scan within the warp
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
-    }
-    if (lane == 31) warp_sum[wid] = incl;
-    __syncthreads();
-    int base = carry;
-    for (int w = 0; w < wid; ++w) base += warp_sum[w];
-    base += incl - nrt;  // route tiles before this expert's
-    for (int j = 0; j < nrt; ++j) {
-      const int c = min(kNT, cnt - j * kNT);
-      for (int m = 0; m < ug_mtiles; ++m) {
-        const int idx = (base + j) * ug_mtiles + m;
-        if (idx < max_ug) ug[idx] = TcTile{e, m, beg + j * kNT, c};
-      }
-      for (int m = 0; m < dn_mtiles; ++m) {
-        const int idx = (base + j) * dn_mtiles + m;
-        if (idx < max_dn) dn[idx] = TcTile{e, m, beg + j * kNT, c};
-      }
-    }
-    __syncthreads();
-    if (tid == kTileThreads - 1) carry = base + nrt;
-    __syncthreads();
-  }
-  if (tid == 0) {
-    counts[0] = min(carry * ug_mtiles, max_ug);
-    counts[1] = min(carry * dn_mtiles, max_dn);
-  }
-}
-
 // x rows in route order as fp16 (zero beyond H); out-of-range magnitudes
 // flag an overflow.
 template <typename XT>
@@ -525,9 +419,15 @@ __global__ void gather_x16_kernel(const XT *__restrict__ x, const int *__restric
   *reinterpret_cast<uint4 *>(x16 + row * Hp + c8 * 8) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+int g_sms_tc = 0;
+
+}  // namespace
+
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::mutex g_encode_mu;
-int g_sms_tc = 0;
+}  // namespace
+
 
 cudaError_t get_encode() {
   std::lock_guard<std::mutex> lock(g_encode_mu);
@@ -545,6 +445,8 @@ cudaError_t get_encode() {
 cudaError_t encode_2d(CUtensorMap *map, CUtensorMapDataType dt, void *base, uint64_t inner,
                       uint64_t rows, uint64_t row_pitch, uint32_t box_inner, uint32_t box_rows,
                       CUtensorMapSwizzle swz) {
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {row_pitch};
   cuuint32_t box[2] = {box_inner, box_rows};
@@ -554,11 +456,10 @@ cudaError_t encode_2d(CUtensorMap *map, CUtensorMapDataType dt, void *base, uint
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-size_t tc_smem() {
+static size_t tc_smem() {
   return 1024 + (size_t)kAStages * kAStage + (size_t)kBStages * kBTile + (size_t)kLabStages * kLabStage;
 }
 
-}  // namespace
 
 int tc_max_tiles(const Layer &L, bool up_gate) {
   const int64_t route_tiles = (int64_t)L.max_routes / kNT + L.E + L.S;
@@ -600,14 +501,7 @@ cudaError_t tc_prepare(Layer &L) {
 cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int T,
                               cudaStream_t stream, cudaEvent_t *ev) {
   const int max_rows = T * L.k + L.S * T;
-  // tile lists
-  build_tiles_kernel<<<1, kTileThreads, 0, stream>>>(L.offsets, L.active, L.E + L.S, L.Fp / kTM,
-                                                     L.Hp / kRowsTile, L.tiles_ug, L.tiles_dn,
-                                                     L.tile_counts, tc_max_tiles(L, true),
-                                                     tc_max_tiles(L, false));
-  count_launches(1);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   // gather x in route order as fp16
   const int64_t chunks = (int64_t)max_rows * (L.Hp / 8);
   const int gb = (int)((chunks + 255) / 256);

@@ -14,6 +14,8 @@
 // selected; w = scale * s / sum(s).
 #include <float.h>
 
+#include <algorithm>
+
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -90,11 +92,15 @@ constexpr int kTM = 32, kTN = 64, kKC = 32;
 // once, not once per chunk.  x is kept token-major and Wr transposed to
 // k-major in shared memory: every inner step is two 16-byte x reads
 // (broadcast within the warp) and four 16-byte Wr reads for 32 FMAs.
+// blockIdx.z = K part: columns [z*kc, (z+1)*kc) of H; part z's partial sums
+// go to logits + z * T * E (a bias, if given, with part 0), summed by the
+// top-k kernel in part order.  Splitting K gives several CTAs per SM at
+// prefill sizes.
 template <typename XT>
 __global__ void __launch_bounds__(256) router_logits_tiled(const XT *__restrict__ x, int T, int H,
                                                            const float *__restrict__ wr, int E,
                                                            const float *__restrict__ bias,
-                                                           int64_t bstride,
+                                                           int64_t bstride, int kc,
                                                            float *__restrict__ logits) {
   __shared__ __align__(16) float xs[kTM][kKC + 4];
   __shared__ __align__(16) float ws[kKC][kTN + 4];
@@ -107,14 +113,19 @@ __global__ void __launch_bounds__(256) router_logits_tiled(const XT *__restrict_
   const bool xv_ok = t0 + lt < T, wv_ok = e0 + le < E;
   const XT *xp = x + (int64_t)(t0 + lt) * H + lk;
   const float *wp = wr + (int64_t)(e0 + le) * H + lw;
+  const int kb = blockIdx.z * kc, ke = min(H, kb + kc);
+  logits += (int64_t)blockIdx.z * T * E;
+  if (blockIdx.z != 0) bias = nullptr;
   float4 xr = make_float4(0.f, 0.f, 0.f, 0.f), wr0 = xr, wr1 = xr;
-  if (xv_ok) xr = load_x4<XT>(xp);
-  if (wv_ok) {
-    wr0 = *reinterpret_cast<const float4 *>(wp);
-    wr1 = *reinterpret_cast<const float4 *>(wp + 4);
+  if (kb < ke) {
+    if (xv_ok) xr = load_x4<XT>(xp + kb);
+    if (wv_ok) {
+      wr0 = *reinterpret_cast<const float4 *>(wp + kb);
+      wr1 = *reinterpret_cast<const float4 *>(wp + kb + 4);
+    }
   }
   float acc[2][4] = {};
-  for (int k0 = 0; k0 < H; k0 += kKC) {
+  for (int k0 = kb; k0 < ke; k0 += kKC) {
     *reinterpret_cast<float4 *>(&xs[lt][lk]) = xr;
     ws[lw + 0][le] = wr0.x;
     ws[lw + 1][le] = wr0.y;
@@ -125,7 +136,7 @@ __global__ void __launch_bounds__(256) router_logits_tiled(const XT *__restrict_
     ws[lw + 6][le] = wr1.z;
     ws[lw + 7][le] = wr1.w;
     __syncthreads();
-    if (k0 + kKC < H) {  // next chunk in flight during this one's FMAs
+    if (k0 + kKC < ke) {  // next chunk in flight during this one's FMAs
       if (xv_ok) xr = load_x4<XT>(xp + k0 + kKC);
       if (wv_ok) {
         wr0 = *reinterpret_cast<const float4 *>(wp + k0 + kKC);
@@ -168,9 +179,12 @@ __global__ void __launch_bounds__(256) router_logits_tiled(const XT *__restrict_
 }
 
 // One warp per token.  E <= 256: lane holds experts lane + 32*i, i < 8.
-__global__ void __launch_bounds__(256) router_topk_kernel(const float *__restrict__ logits, int T,
-                                                          int E, int k, float scale,
-                                                          int32_t *__restrict__ ids,
+// The logits are the sum of `parts` K-partial arrays, added in part order,
+// plus the optional bias b[t][e] (row stride bstride; 0 = one row for all).
+__global__ void __launch_bounds__(256) router_topk_kernel(const float *__restrict__ logits, int parts,
+                                                          const float *__restrict__ bias,
+                                                          int64_t bstride, int T, int E, int k,
+                                                          float scale, int32_t *__restrict__ ids,
                                                           float *__restrict__ weights) {
   const int lane = threadIdx.x & 31;
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -179,7 +193,12 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    float l = e < E ? logits[(int64_t)t * E + e] : -FLT_MAX;
+    float l = -FLT_MAX;
+    if (e < E) {
+      l = logits[(int64_t)t * E + e];
+      for (int z = 1; z < parts; ++z) l += logits[(int64_t)z * T * E + (int64_t)t * E + e];
+      if (bias) l += bias[(int64_t)t * bstride + e];
+    }
     v[i] = (l == l) ? l : -FLT_MAX;  // NaN never wins
   }
   unsigned taken = 0;
@@ -221,9 +240,14 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
 
 }  // namespace
 
+int router_parts(int T, int max_parts) {
+  return T <= 16 ? 1 : std::max(1, std::min(max_parts, kRouterMaxParts));
+}
+
 cudaError_t launch_router_logits(const Layer &L, const void *x, moe_dtype xdt, int T,
-                                 const float *wr, const float *bias, int64_t bias_stride,
-                                 float *logits, cudaStream_t stream) {
+                                 const float *wr, float *logits, int parts, cudaStream_t stream) {
+  const float *bias = nullptr;  // added by the top-k kernel
+  const int64_t bias_stride = 0;
   if (T <= 16) {
     dim3 grid((L.E + 7) / 8);
     if (xdt == MOE_DT_BF16)
@@ -233,24 +257,26 @@ cudaError_t launch_router_logits(const Layer &L, const void *x, moe_dtype xdt, i
       router_logits_small<float><<<grid, 256, 0, stream>>>((const float *)x, T, L.H, wr, L.E,
                                                            bias, bias_stride, logits);
   } else {
-    dim3 grid((T + kTM - 1) / kTM, (L.E + kTN - 1) / kTN);
+    const int kc = ((L.H + parts - 1) / parts + kKC - 1) / kKC * kKC;
+    dim3 grid((T + kTM - 1) / kTM, (L.E + kTN - 1) / kTN, parts);
     if (xdt == MOE_DT_BF16)
       router_logits_tiled<__nv_bfloat16><<<grid, 256, 0, stream>>>(
-          (const __nv_bfloat16 *)x, T, L.H, wr, L.E, bias, bias_stride, logits);
+          (const __nv_bfloat16 *)x, T, L.H, wr, L.E, bias, bias_stride, kc, logits);
     else
       router_logits_tiled<float><<<grid, 256, 0, stream>>>((const float *)x, T, L.H, wr, L.E,
-                                                           bias, bias_stride, logits);
+                                                           bias, bias_stride, kc, logits);
   }
   count_launches(1);
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_topk(const Layer &L, const float *logits, int T, int32_t *ids,
-                               float *weights, cudaStream_t stream) {
+cudaError_t launch_router_topk(const Layer &L, const float *logits, int parts, const float *bias,
+                               int64_t bias_stride, int T, int32_t *ids, float *weights,
+                               cudaStream_t stream) {
   const int warps_per_block = 8;
   const int blocks = (T + warps_per_block - 1) / warps_per_block;
-  router_topk_kernel<<<blocks, 32 * warps_per_block, 0, stream>>>(logits, T, L.E, L.k, L.scale,
-                                                                  ids, weights);
+  router_topk_kernel<<<blocks, 32 * warps_per_block, 0, stream>>>(logits, parts, bias, bias_stride, T,
+                                                                  L.E, L.k, L.scale, ids, weights);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -338,8 +364,10 @@ extern "C" moe_status moe_route_noalloc(const void *x, moe_dtype x_dtype, int32_
   L.k = top_k;
   L.scale = routed_scaling;
   cudaStream_t st = (cudaStream_t)stream;
-  e = moe::launch_router_logits(L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, logits, st);
-  if (e == cudaSuccess) e = moe::launch_router_topk(L, logits, T, ids, weights, st);
+  const int parts = moe::router_parts(T, (int)(moe::kNoAllocMaxLogits / ((int64_t)T * n_experts)));
+  e = moe::launch_router_logits(L, x, x_dtype, T, router_w, logits, parts, st);
+  if (e == cudaSuccess)
+    e = moe::launch_router_topk(L, logits, parts, logit_bias, bias_row_stride, T, ids, weights, st);
   if (e != cudaSuccess) return report_error(MOE_ERR_CUDA, "moe_route_noalloc: %s", cudaGetErrorString(e));
   return MOE_OK;
 }

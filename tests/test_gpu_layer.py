@@ -266,3 +266,24 @@ def test_graph_replay_matches_eager():
     L.check()
     for i in range(len(xs)):
         assert torch.allclose(outs[i].float().cpu(), eager[i], rtol=0, atol=2e-2 * eager[i].abs().max().item())
+
+
+@pytest.mark.parametrize("H,E,k,T,zipf", [(256, 8, 2, 256, False), (288, 100, 8, 300, True),
+                                          (3584, 64, 4, 512, False)])
+def test_large_batch_router_bit_exact(H, E, k, T, zipf):
+    """Batches of >= 256 bf16 tokens take the tensor-core router (the fp32
+    router rows split into three exact bf16 parts): ids must still equal
+    the fp64 oracle's bit for bit; E > 64 exercises two rows per splitting
+    thread, H = 288 a K tail that is half a 64-wide step."""
+    wl = synth.Workload(f"router: H {H}, E {E}, top-{k}, {T} tokens", H, E, k, 32, T, "bf16", 0.05,
+                        zipf=zipf)
+    ew = synth.expert_weights(0, 0, E, H, 32)
+    c = cases.make_case(wl, ew=ew)
+    L = MoeLayer.from_weights(ew, k=k, scale=wl.scale, max_tokens=T)
+    x, wr, bias = _dev_inputs(c)
+    ids, w = L.route(x, wr, bias)
+    torch.cuda.synchronize()
+    L.check()
+    np.testing.assert_array_equal(ids.cpu().numpy(), c.ids)
+    np.testing.assert_allclose(w.cpu().numpy(), c.w, rtol=0, atol=2e-6)
+    L.close()
