@@ -10,7 +10,7 @@
 // step there was launch-bound, with the card idle three quarters of the time.)
 //
 // Grid: one CTA per SM (its shared memory forces 1 CTA/SM).  Each CTA has
-// 16 consumer warps and one producer warp:
+// 24 consumer warps and one producer warp:
 //   producer  issues 1D bulk (TMA) copies of weight rows into a ring of
 //             32 KB shared-memory stages (full/empty mbarriers per stage);
 //             before the programmatic-dependent-launch wait it already
@@ -21,9 +21,10 @@
 //             up/gate rows and this CTA's rows of every W_down.
 //   consumers stage x, compute the router logit of expert `blockIdx.x`,
 //             quantise x to 16-bit integers per 32-block (power-of-two
-//             scale), stream the up/gate items (warp w: gate row (w < 8) or
-//             up row of output f0 + w % 8; the two meet through a named
-//             barrier for SwiGLU and write h to global memory), wait
+//             scale), stream the up/gate items (three groups of 8 warps
+//             take alternate items; warp w computes the gate and the up row
+//             of output f0 + w % 8, applies SwiGLU and writes h to global
+//             memory), wait
 //             (bounded) until every CTA has written its h, then own output
 //             rows [c*H/G, (c+1)*H/G): every consumer thread keeps fixed
 //             (row, 16-weight) units of W_down, accumulates them over all
@@ -44,7 +45,9 @@
 namespace moe {
 namespace {
 
-constexpr int kConsumerWarps = 16;
+constexpr int kGroupWarps = 8;      // one up/gate item: 8 warps, one output each
+constexpr int kItemGroups = 3;      // up/gate items in work at once
+constexpr int kConsumerWarps = kGroupWarps * kItemGroups;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr int kProducerWarp = kConsumerWarps;
@@ -505,18 +508,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     named_sync(kBarConsumers, kConsumers);
 
     // One up/gate item (gate rows of up to fpi outputs in the stage's first
-    // half, their up rows in the second) is taken by one half of the
-    // consumer warps -- items alternate between the halves, so two items
-    // are in work at once.  Warp w computes both rows of output f0 + (w & 7):
+    // half, their up rows in the second) is taken by one group of 8 consumer
+    // warps -- items rotate among the kItemGroups groups, so that many items
+    // are in work at once.  Warp w computes both rows of output f0 + (w % 8):
     // every activation load serves the gate and the up row, and SwiGLU is
-    // applied inside the warp.  Each of the 8 warps arrives twice on the
-    // stage's "empty" barrier (its count is the 16 consumer warps).
+    // applied inside the warp.  Each of the 8 warps arrives kItemGroups times
+    // on the stage's "empty" barrier (its count is all the consumer warps).
     auto process_upgate = [&](int i) {
       const Item it = items[i];
       const int s = i % nst;
       if (!mbar_wait_sleep(&full_bar[s], (uint32_t)(i / nst) & 1u, kPollLimit, 32)) atomicOr(&status, 2);
       const int rs = ex_rs[it.a], nr = ex_rs[it.a + 1] - rs;
-      const int fl = warp & 7;
+      const int fl = warp % kGroupWarps;
       float accg[TT], accu[TT];
 #pragma unroll
       for (int r = 0; r < TT; ++r) accg[r] = accu[r] = 0.f;
@@ -586,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_cnt(&empty_bar[s], 2);  // for this warp and its idle twin
+      if (lane == 0) mbar_arrive_cnt(&empty_bar[s], kItemGroups);  // for this warp and its idle twins
       if (fl < it.count) {
 #pragma unroll
         for (int r = 0; r < TT; ++r) {
@@ -599,13 +602,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     };
 
     int i = 0;
-    const int my_half = warp >> 3;  // up/gate items alternate between the warp halves
+    const int my_group = warp / kGroupWarps;  // up/gate items rotate among the warp groups
     for (; i < n_shared_items; ++i)
-      if ((i & 1) == my_half) process_upgate(i);
+      if (i % kItemGroups == my_group) process_upgate(i);
     if (!mbar_wait_sleep(&plan_bar, 0, kPollLimit, 128)) atomicOr(&status, 2);
     if (!(status & 1)) {
       for (; i < n_items && items[i].kind == 0; ++i)
-        if ((i & 1) == my_half) process_upgate(i);
+        if (i % kItemGroups == my_group) process_upgate(i);
 
       // ---- every CTA's h written ----
       named_sync(kBarConsumers, kConsumers);
@@ -809,10 +812,12 @@ bool plan_fused(const Layer &L, int T, FusedPlan &fp) {
   const size_t fixed = (size_t)T * L.Hp * 2 + (size_t)T * (L.Hp / 32) * 4;
   const size_t limit = smem_limit_fused();
   if (fixed + (size_t)T * per_route + 3 * (size_t)kStage > limit) return false;
-  // an even number of stages: up/gate items alternate between the two
-  // consumer-warp halves, and a half's parity wait on a stage is only exact
-  // when the stage's previous use was that half's too
-  fp.nstage = (int)std::min<size_t>(kMaxStages, (limit - fixed - (size_t)T * per_route) / kStage) & ~1;
+  // a multiple of kItemGroups stages: up/gate items rotate among the
+  // consumer-warp groups, and a group's parity wait on a stage is only
+  // exact when the stage's previous use was that group's too
+  fp.nstage = (int)std::min<size_t>(kMaxStages, (limit - fixed - (size_t)T * per_route) / kStage);
+  fp.nstage -= fp.nstage % kItemGroups;
+  if (fp.nstage < kItemGroups) return false;
   const size_t left = limit - fixed - (size_t)fp.nstage * kStage;
   fp.hq_cap = (int)std::min<size_t>((size_t)T * (L.k + L.S), left / per_route);
   fp.smem = fixed + (size_t)fp.nstage * kStage + (size_t)fp.hq_cap * per_route;
