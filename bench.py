@@ -86,6 +86,20 @@ def bench_config(args, wl, world):
         "graph_steps": G}
 
 
+def replay_percentiles(start, marks, per_replay_steps):
+    """p10 / median / p90 of the per-step time over the graph replays of the
+    timed region (each replay holds per_replay_steps steps), in ms."""
+    if not marks:
+        return None
+    ts, prev = [], start
+    for m in marks:
+        ts.append(prev.elapsed_time(m) / per_replay_steps)
+        prev = m
+    ts.sort()
+    pick = lambda q: ts[min(len(ts) - 1, int(q * (len(ts) - 1) + 0.5))]
+    return {"p10": pick(0.1), "median": pick(0.5), "p90": pick(0.9), "replays": len(ts)}
+
+
 def algorithmic_bytes(T, distinct_experts):
     """HBM bytes one call must move at least: the selected experts' and the
     shared expert's IQ4_NL weights, the fp32 router, x in and out (bf16)."""
@@ -263,11 +277,13 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
     with Clocks(local_rank) as clk:
         with torch.cuda.stream(stream):
             start.record(stream)
-            for _ in range(reps):
+            for i in range(reps):
                 g_main.replay()
+                marks[i].record(stream)
             if g_rem:
                 g_rem.replay()
             stop.record(stream)
@@ -374,6 +390,7 @@ def run_ours(args, rank, world, local_rank):
         "expert_weight_frac_of_hbm_peak": expert_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
         "roofline": roofline,
         "stage_ms": stage_ms,
+        "step_ms_percentiles": replay_percentiles(start, marks, G),
         "gpu_launches": gpu_launches,
         "clocks": clk.summary(),
         "e2e": e2e,
@@ -441,11 +458,13 @@ def run_trunk(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
     with Clocks(local_rank) as clk:
         with torch.cuda.stream(stream):
             start.record(stream)
-            for _ in range(reps):
+            for i in range(reps):
                 g_main.replay()
+                marks[i].record(stream)
             if g_rem:
                 g_rem.replay()
             stop.record(stream)
@@ -506,6 +525,7 @@ def run_trunk(args, rank, world, local_rank):
         "us_per_layer": ms_per_step * 1e3 / NL,
         "expert_weight_gbs": expert_bytes / (ms_per_step * 1e-3) / 1e9,
         "expert_weight_frac_of_hbm_peak": expert_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
+        "step_ms_percentiles": replay_percentiles(start, marks, G),
         "roofline": {"bound": "hbm", "kernel": f"whole trunk step ({NL} layers, all launches)",
                      "achieved": achieved, "peak": hbm_peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": achieved / hbm_peak,

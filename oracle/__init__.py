@@ -64,6 +64,8 @@ def _configure(lib):
     lib.oracle_iq4nl_quantize.restype = None
     lib.oracle_route.argtypes = [I, I, I, I, D, P, P, P, I, P, P, P]
     lib.oracle_route.restype = ctypes.c_int
+    lib.oracle_route_selbias.argtypes = [I, I, I, I, D, P, P, P, I, P, P, P]
+    lib.oracle_route_selbias.restype = ctypes.c_int
     lib.oracle_moe_forward.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P]
     lib.oracle_moe_forward.restype = ctypes.c_int
     lib.oracle_rmsnorm.argtypes = [I, I, P, D, P]
@@ -148,6 +150,34 @@ def route(x: np.ndarray, wr: np.ndarray, k: int, scale: float = 2.0,
     if rc != 0:
         raise ValueError(f"oracle_route: invalid sizes (rc={rc})")
     return ids, w, logits
+
+
+def route_selbias(x: np.ndarray, wr: np.ndarray, k: int, scale: float, sel_bias: np.ndarray):
+    """Sigmoid top-k router whose bias only steers the selection (noaux_tc):
+    experts chosen by sigmoid(l) + b, weights from sigmoid(l).  sel_bias
+    [T,E] or [E].  Returns (ids, weights, logits)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    wr = np.ascontiguousarray(wr, dtype=np.float64)
+    T, H = x.shape
+    E = wr.shape[0]
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    logits = np.empty((T, E), dtype=np.float64)
+    b = np.ascontiguousarray(sel_bias, dtype=np.float64)
+    rc = _load().oracle_route_selbias(T, H, E, k, float(scale), _p(x), _p(wr), _p(b),
+                                      E if b.ndim == 2 else 0, _p(logits), _p(ids), _p(w))
+    if rc != 0:
+        raise ValueError(f"oracle_route_selbias: invalid sizes (rc={rc})")
+    return ids, w, logits
+
+
+def min_selection_gap(logits: np.ndarray, sel_bias: np.ndarray, k: int) -> np.ndarray:
+    """Per token, the smallest gap between adjacent selection keys
+    sigmoid(l) + b among the k+1 largest (fp64)."""
+    s = 1.0 / (1.0 + np.exp(-np.asarray(logits, np.float64)))
+    key = s + np.asarray(sel_bias, np.float64)
+    top = -np.sort(-key, axis=1)[:, :k + 1]
+    return np.min(top[:, :-1] - top[:, 1:], axis=1)
 
 
 def moe_forward(x: np.ndarray, ids: np.ndarray, weights: np.ndarray, ew) -> np.ndarray:

@@ -151,6 +151,53 @@ int oracle_route(int64_t T, int64_t H, int64_t E, int64_t k, double scale,
 }
 
 /*
+ * Router with a selection-only score bias (noaux_tc) [EPQ "模型與路由":
+ * "sigmoid + ffn_exp_probs_b (noaux_tc)"; the bias is a per-expert vector
+ * added to the sigmoid probabilities].  Per token t:
+ *   l_e = x_t . Wr_e                  s_e = 1 / (1 + exp(-l_e))
+ *   the k experts with the largest s_e + b[t, e], in descending order of
+ *   that sum, equal sums going to the lower expert id
+ *   w_e = scale * s_e / sum over the selected of s   (the unbiased scores)
+ * b[t, e] = bias[t * bias_stride + e] (bias_stride 0: one vector for all).
+ * logits (may be NULL) receive l.  Returns 0, or -1 on invalid sizes.
+ */
+int oracle_route_selbias(int64_t T, int64_t H, int64_t E, int64_t k, double scale,
+                         const double *x, const double *wr, const double *bias,
+                         int64_t bias_stride, double *logits, int32_t *ids,
+                         double *weights) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0 || k > E || !bias) return -1;
+  double *prob = (double *)malloc(sizeof(double) * (size_t)E);
+  double *choice = (double *)malloc(sizeof(double) * (size_t)E);
+  char *taken = (char *)malloc((size_t)E);
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int64_t h = 0; h < H; ++h) acc += x[t * H + h] * wr[e * H + h];
+      prob[e] = sigmoid(acc);
+      choice[e] = prob[e] + bias[t * bias_stride + e];
+      taken[e] = 0;
+      if (logits) logits[t * E + e] = acc;
+    }
+    double sum = 0.0;
+    for (int64_t j = 0; j < k; ++j) {
+      int64_t best = -1;
+      for (int64_t e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || choice[e] > choice[best]) best = e;
+      }
+      taken[best] = 1;
+      ids[t * k + j] = (int32_t)best;
+      sum += prob[best];
+    }
+    for (int64_t j = 0; j < k; ++j) weights[t * k + j] = scale * prob[ids[t * k + j]] / sum;
+  }
+  free(prob);
+  free(choice);
+  free(taken);
+  return 0;
+}
+
+/*
  * Layer forward with given routes [EPQ "整層"; REC section 2; ZHU "FFN"]:
  *   out[t] = sum_j weights[t,j] * FFN_{ids[t,j]}(x[t]) + FFN_shared(x[t])
  *   FFN(x) = W_down (silu(W_gate x) * (W_up x)),  silu(g) = g / (1 + e^-g)

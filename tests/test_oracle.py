@@ -264,11 +264,50 @@ def pin_invalid_ids_rejected():
         oracle.moe_forward(x, np.array([[0, 8]] * 3, dtype=np.int32), np.ones((3, 2)), ew)
 
 
+def pin_selection_bias_hand_case():
+    """noaux_tc [EPQ "模型與路由": sigmoid + ffn_exp_probs_b]: the bias moves
+    expert 1 ahead of expert 0, the weights stay the unbiased scores."""
+    x = np.array([[1.0]])
+    wr = np.array([[2.0], [1.0], [0.0]])                 # l = 2, 1, 0
+    s = 1.0 / (1.0 + np.exp(-np.array([2.0, 1.0, 0.0])))  # 0.8808, 0.7311, 0.5
+    b = np.array([0.0, 0.2, 0.0])                        # keys 0.8808, 0.9311, 0.5
+    ids, w, _ = oracle.route_selbias(x, wr, 2, 2.0, b)
+    assert ids.tolist() == [[1, 0]]
+    np.testing.assert_allclose(w[0], 2.0 * np.array([s[1], s[0]]) / (s[1] + s[0]), rtol=1e-15)
+    ids1, w1, _ = oracle.route_selbias(x, wr, 1, 2.0, b)
+    assert ids1.tolist() == [[1]] and w1[0, 0] == 2.0
+    # equal keys go to the lower id: b makes expert 2's key equal expert 1's
+    b2 = np.array([-1.0, 0.0, s[1] - s[2]])
+    ids2, _, _ = oracle.route_selbias(x, wr, 1, 2.0, b2)
+    assert ids2.tolist() == [[1]]
+
+
+def pin_selection_bias_zero_and_forcing():
+    """b = 0 is the plain router; a large bias on one expert puts it first
+    for every token without changing the other weights' ratios."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((6, 32))
+    wr = rng.standard_normal((8, 32)) * 0.3
+    ids0, w0, _ = oracle.route(x, wr, 3, 2.0)
+    ids1, w1, l1 = oracle.route_selbias(x, wr, 3, 2.0, np.zeros(8))
+    np.testing.assert_array_equal(ids1, ids0)
+    np.testing.assert_array_equal(w1, w0)
+    b = np.zeros(8)
+    b[5] = 10.0
+    ids2, w2, _ = oracle.route_selbias(x, wr, 3, 2.0, b)
+    assert (ids2[:, 0] == 5).all()
+    s = 1.0 / (1.0 + np.exp(-l1))
+    for t in range(6):
+        sel = s[t, ids2[t]]
+        np.testing.assert_allclose(w2[t], 2.0 * sel / sel.sum(), rtol=1e-14)
+
+
 PINS = [pin_fp16_values, pin_golden_blocks, pin_matrix_bytes, pin_roundtrip,
         pin_router_hand_case, pin_router_brute_force, pin_weights_sum_to_scale,
         pin_rank_one_closed_form, pin_all_experts_equals_dense, pin_top1_special_case,
         pin_permutation_and_token_independence, pin_zero_weight_route_contributes_nothing,
-        pin_rmsnorm_closed_form, pin_invalid_ids_rejected]
+        pin_rmsnorm_closed_form, pin_invalid_ids_rejected, pin_selection_bias_hand_case,
+        pin_selection_bias_zero_and_forcing]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -297,6 +336,10 @@ MUTANTS = {
     "down transposed": ("wd[r * F + f]", "wd[f * H + r]"),
     "route weight dropped": ("ot[r] += wt[i] * y", "ot[r] += y"),
     "rmsnorm mean": ("ss / (double)H", "ss / (double)(H - 1)"),
+    "selection bias subtracted": ("choice[e] = prob[e] + bias", "choice[e] = prob[e] - bias"),
+    "selection by smallest key": ("choice[e] > choice[best]", "choice[e] < choice[best]"),
+    "selection bias in the weights": ("sum += prob[best]", "sum += choice[best]"),
+    "selection bias ignored": ("choice[e] = prob[e] + bias[t * bias_stride + e]", "choice[e] = prob[e]"),
 }
 
 
