@@ -67,7 +67,8 @@ typedef enum { MOE_DT_BF16 = 0, MOE_DT_FP32 = 1 } moe_dtype;
 
 /* Layer shape.  Limits: hidden and expert_ffn multiples of 32 in [32, 16384];
  * 1 <= n_experts <= 256; 1 <= top_k <= min(n_experts, 8); n_shared 0 or 1;
- * 1 <= max_tokens <= 65536; routed_scaling > 0; flags must be 0. */
+ * 1 <= max_tokens <= 65536; routed_scaling > 0; flags a combination of the
+ * MOE_FLAG_* bits below (other bits: MOE_ERR_INVALID_ARG). */
 typedef struct {
   int32_t hidden;       /* H                                                */
   int32_t n_experts;    /* E routed experts                                 */
@@ -76,8 +77,18 @@ typedef struct {
   int32_t n_shared;     /* 1: one always-on shared expert, weight 1         */
   float routed_scaling; /* scale applied to the renormalised weights        */
   int32_t max_tokens;   /* largest T any later call may pass                */
-  uint32_t flags;       /* reserved, must be 0                              */
+  uint32_t flags;       /* MOE_FLAG_* bits, 0 for the plain router          */
 } moe_shapes;
+
+/* Selection-only score bias (noaux_tc) [EPQ, "模型與路由": sigmoid plus the
+ * per-expert probability bias ffn_exp_probs_b].  With this flag the
+ * logit_bias argument of moe_route and moe_layer_forward_routed is not added
+ * to the logits: expert e is ranked by sigmoid(l_e) + b_e, while the weights
+ * are still routed_scaling * s_e / sum(s) of the unbiased s_e = sigmoid(l_e).
+ * Without it the bias is added to the logit before the sigmoid and so enters
+ * both the ranking and the weights.  moe_route_noalloc has no layer and always
+ * takes the logit reading. */
+#define MOE_FLAG_SELECTION_BIAS 1u
 
 /* Expert weights in IQ4_NL blocks (18 bytes each, no alignment needed).
  *   up, gate: [E][F][H/32] blocks     down: [E][H][F/32] blocks
@@ -112,7 +123,8 @@ moe_status moe_layer_destroy(moe_layer_t layer);
  *   router_w    [E][H] fp32, 16-byte aligned (the layer's ffn_gate_inp)
  *   logit_bias  NULL, or fp32 with row t at logit_bias + t*bias_row_stride
  *               (stride 0: one [E] row for every token), 16-byte aligned;
- *               added to the logit before the sigmoid
+ *               added to the logit before the sigmoid, or with
+ *               MOE_FLAG_SELECTION_BIAS to the sigmoid score for ranking only
  *   ids         [T][k] int32 out, descending score; equal scores -> lower id
  *   weights     [T][k] fp32 out, sum to routed_scaling per token
  * 0 <= T <= max_tokens; T == 0 returns MOE_OK and launches nothing. */

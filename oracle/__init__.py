@@ -176,7 +176,10 @@ def min_selection_gap(logits: np.ndarray, sel_bias: np.ndarray, k: int) -> np.nd
     sigmoid(l) + b among the k+1 largest (fp64)."""
     s = 1.0 / (1.0 + np.exp(-np.asarray(logits, np.float64)))
     key = s + np.asarray(sel_bias, np.float64)
-    top = -np.sort(-key, axis=1)[:, :k + 1]
+    kk = min(k + 1, key.shape[1])
+    if kk < 2:
+        return np.full(key.shape[0], np.inf)
+    top = -np.sort(-key, axis=1)[:, :kk]
     return np.min(top[:, :-1] - top[:, 1:], axis=1)
 
 

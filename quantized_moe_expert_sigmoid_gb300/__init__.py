@@ -18,6 +18,7 @@ from .build import LIB as _LIB_PATH
 MOE_OK = 0
 MOE_DT_BF16 = 0
 MOE_DT_FP32 = 1
+MOE_FLAG_SELECTION_BIAS = 1  # the bias ranks experts only (noaux_tc); weights stay unbiased
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_OUT_OF_MEMORY", 5: "MOE_ERR_CUDA",
@@ -140,11 +141,11 @@ def _stream(stream):
 
 def moe_layer_create(hidden, n_experts, top_k, expert_ffn, n_shared, routed_scaling,
                      max_tokens, up, gate, down, sh_up=None, sh_gate=None, sh_down=None,
-                     stream=None):
+                     stream=None, flags=0):
     """Returns an opaque handle (int).  Weight tensors: uint8 on the GPU in
-    the IQ4_NL block layout of include/moe_gb300.h."""
+    the IQ4_NL block layout of include/moe_gb300.h; flags: MOE_FLAG_* bits."""
     lib = load_library()
-    sh = _Shapes(hidden, n_experts, top_k, expert_ffn, n_shared, routed_scaling, max_tokens, 0)
+    sh = _Shapes(hidden, n_experts, top_k, expert_ffn, n_shared, routed_scaling, max_tokens, flags)
     w = _Weights(*(_ptr(t, n, _dt()["u8"]) for t, n in ((up, "up"), (gate, "gate"), (down, "down"),
                                                          (sh_up, "sh_up"), (sh_gate, "sh_gate"),
                                                          (sh_down, "sh_down"))))
@@ -278,15 +279,15 @@ class MoeLayer:
 
     def __init__(self, hidden, n_experts, top_k, expert_ffn, n_shared=1, routed_scaling=2.0,
                  max_tokens=1, *, up, gate, down, sh_up=None, sh_gate=None, sh_down=None,
-                 stream=None):
+                 stream=None, flags=0):
         self.H, self.E, self.k, self.F, self.S = hidden, n_experts, top_k, expert_ffn, n_shared
-        self.scale, self.max_tokens = routed_scaling, max_tokens
+        self.scale, self.max_tokens, self.flags = routed_scaling, max_tokens, flags
         self.handle = moe_layer_create(hidden, n_experts, top_k, expert_ffn, n_shared,
                                        routed_scaling, max_tokens, up, gate, down, sh_up,
-                                       sh_gate, sh_down, stream)
+                                       sh_gate, sh_down, stream, flags)
 
     @classmethod
-    def from_weights(cls, ew, k, scale=2.0, max_tokens=1, device="cuda", stream=None):
+    def from_weights(cls, ew, k, scale=2.0, max_tokens=1, device="cuda", stream=None, flags=0):
         """Upload synth.ExpertWeights-like numpy arrays and create the layer."""
         import torch
         t = lambda a: None if a is None else torch.from_numpy(a).to(device)
@@ -295,7 +296,7 @@ class MoeLayer:
         S = 0 if getattr(ew, "sh_up", None) is None else 1
         return cls(H, E, k, F, S, scale, max_tokens, up=t(ew.up), gate=t(ew.gate), down=t(ew.down),
                    sh_up=t(ew.sh_up) if S else None, sh_gate=t(ew.sh_gate) if S else None,
-                   sh_down=t(ew.sh_down) if S else None, stream=stream)
+                   sh_down=t(ew.sh_down) if S else None, stream=stream, flags=flags)
 
     def route(self, x, router_w, logit_bias=None, stream=None):
         import torch

@@ -234,11 +234,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
       // ---- top-k of every token (every CTA computes the same selection) ----
       for (int t = 0; t < T; ++t) {
         if (do_route) {
+          // selection key: the logit (any bias already added), or in
+          // selection mode the sigmoid score plus the bias
           float v[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int e = lane + 32 * i;
-            const float l = e < E ? __ldcg(&L.logits[(int64_t)t * E + e]) : -FLT_MAX;
+            float l = e < E ? __ldcg(&L.logits[(int64_t)t * E + e]) : -FLT_MAX;
+            if (L.sel_bias && e < E) {
+              l = 1.0f / (1.0f + expf(-l));
+              if (p.bias) l += p.bias[(int64_t)t * p.bstride + e];
+            }
             v[i] = (l == l) ? l : -FLT_MAX;  // NaN never wins
           }
           // k rounds of a warp arg-max on order-preserving integer keys:
@@ -269,8 +275,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
               my_key = m;
             }
           }
-          // the k scores in parallel, lane j holding the j-th
-          const float my_s = lane < K ? 1.0f / (1.0f + expf(-float_from_order_key(my_key))) : 0.f;
+          // the k scores in parallel, lane j holding the j-th (selection
+          // mode: from the winner's unbiased logit)
+          float my_l = float_from_order_key(my_key);
+          if (L.sel_bias && lane < K) {
+            my_l = __ldcg(&L.logits[(int64_t)t * E + my_id]);
+            if (my_l != my_l) my_l = -FLT_MAX;
+          }
+          const float my_s = lane < K ? 1.0f / (1.0f + expf(-my_l)) : 0.f;
           const float ssum = warp_sum(my_s);
           if (lane < K) {
             const float wgt = L.scale * my_s / ssum;
@@ -451,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           for (int t = 0; t < T; ++t) {
             float v = warp_sum(lane < kConsumerWarps ? red[lane][t] : 0.f);
             if (lane == 0) {
-              if (p.bias) v += p.bias[(int64_t)t * p.bstride + e];
+              if (p.bias && !L.sel_bias) v += p.bias[(int64_t)t * p.bstride + e];
               L.logits[(int64_t)t * E + e] = v;
             }
           }

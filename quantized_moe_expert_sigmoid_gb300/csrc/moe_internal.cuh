@@ -52,6 +52,7 @@ struct Layer {
   // shape
   int H, E, k, F, S;  // S = number of shared experts (0 or 1)
   float scale;
+  int sel_bias;              // 1: the bias shifts expert selection only (MOE_FLAG_SELECTION_BIAS)
   int max_tokens;
   int Hp, Fp;                // H and F padded to multiples of 256
   int64_t gu_row_bytes;      // Hp/256 * 144

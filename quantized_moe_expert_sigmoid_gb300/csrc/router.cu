@@ -184,22 +184,32 @@ __global__ void __launch_bounds__(256) router_logits_tiled(const XT *__restrict_
 __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restrict__ logits, int parts,
                                                           const float *__restrict__ bias,
                                                           int64_t bstride, int T, int E, int k,
-                                                          float scale, int32_t *__restrict__ ids,
+                                                          float scale, int sel,
+                                                          int32_t *__restrict__ ids,
                                                           float *__restrict__ weights) {
   const int lane = threadIdx.x & 31;
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
-  float v[8];
+  // selection key per expert: the biased logit (logit mode), or the sigmoid
+  // score plus the bias (selection mode, whose weights use the plain score)
+  float v[8], lraw[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    float l = -FLT_MAX;
+    float l = -FLT_MAX, key = -FLT_MAX;
     if (e < E) {
       l = logits[(int64_t)t * E + e];
       for (int z = 1; z < parts; ++z) l += logits[(int64_t)z * T * E + (int64_t)t * E + e];
-      if (bias) l += bias[(int64_t)t * bstride + e];
+      const float b = bias ? bias[(int64_t)t * bstride + e] : 0.f;
+      if (sel) {
+        key = 1.0f / (1.0f + expf(-l)) + b;
+      } else {
+        l += b;
+        key = l;
+      }
     }
-    v[i] = (l == l) ? l : -FLT_MAX;  // NaN never wins
+    lraw[i] = (l == l) ? l : -FLT_MAX;
+    v[i] = (key == key) ? key : -FLT_MAX;  // NaN never wins
   }
   unsigned taken = 0;
   int my_id = 0;
@@ -225,7 +235,13 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
       }
     }
     if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-    const float s = 1.0f / (1.0f + expf(-best));
+    // the winner's logit, from the lane that holds it
+    float lw = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i == (bid >> 5)) lw = lraw[i];
+    lw = __shfl_sync(0xffffffffu, lw, bid & 31);
+    const float s = 1.0f / (1.0f + expf(-lw));
     ssum += s;
     if (lane == j) {
       my_id = bid;
@@ -276,7 +292,7 @@ cudaError_t launch_router_topk(const Layer &L, const float *logits, int parts, c
   const int warps_per_block = 8;
   const int blocks = (T + warps_per_block - 1) / warps_per_block;
   router_topk_kernel<<<blocks, 32 * warps_per_block, 0, stream>>>(logits, parts, bias, bias_stride, T,
-                                                                  L.E, L.k, L.scale, ids, weights);
+                                                                  L.E, L.k, L.scale, L.sel_bias, ids, weights);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -363,6 +379,7 @@ extern "C" moe_status moe_route_noalloc(const void *x, moe_dtype x_dtype, int32_
   L.E = n_experts;
   L.k = top_k;
   L.scale = routed_scaling;
+  L.sel_bias = 0;  // logit_bias is added to the logits
   cudaStream_t st = (cudaStream_t)stream;
   const int parts = moe::router_parts(T, (int)(moe::kNoAllocMaxLogits / ((int64_t)T * n_experts)));
   e = moe::launch_router_logits(L, x, x_dtype, T, router_w, logits, parts, st);

@@ -226,6 +226,16 @@ def zipf_logit_bias(seed: int, T: int, E: int, s: float = ZIPF_S,
     return (base[None, :] + beta * jit).astype(np.float32)
 
 
+def selection_bias(seed: int, E: int, T: int | None = None, sigma: float = 0.1) -> np.ndarray:
+    """Per-expert selection bias (the noaux_tc probability bias): N(0, sigma)
+    values, [E] fp32, or [T x E] when T is given (one row per token).  Scores
+    are sigmoid outputs in (0, 1), so sigma 0.1 reorders a good share of the
+    close candidates without overriding the router."""
+    shape = (E,) if T is None else (T, E)
+    tag = "selbias" if T is None else "selbias/rows"
+    return (normal(stream_key(seed, tag, E), int(np.prod(shape))).reshape(shape) * sigma).astype(np.float32)
+
+
 # --------------------------------------------------------------------------
 # Workloads
 # --------------------------------------------------------------------------

@@ -365,3 +365,20 @@ def test_planted_mistakes_are_caught():
             if not caught:
                 escaped.append(name)
     assert not escaped, f"mistakes no pin catches: {escaped}"
+
+
+def test_selection_bias_cases_change_routes_and_keep_gaps():
+    """The parity cases with a drawn selection bias: it changes the chosen
+    set of most tokens (so the GPU tests exercise it), every token's k+1
+    largest keys stay >= 1e-4 apart, and the weights, free of the bias,
+    still sum to routed_scaling."""
+    from oracle import cases
+    wl = synth.Workload("selection bias: H 256, E 64, top-4, 64 tokens", 256, 64, 4, 32, 64, "bf16", 0.05)
+    ew = synth.expert_weights(0, 0, wl.E, wl.H, wl.F)
+    for b in (synth.selection_bias(0, wl.E), synth.selection_bias(1, wl.E, wl.T)):
+        c = cases.make_case(wl, ew=ew, selection_bias=b)
+        assert c.selection_bias
+        plain_ids, _, _ = oracle.route(c.x64, c.wr, wl.k, wl.scale)
+        assert (np.sort(plain_ids, 1) != np.sort(c.ids, 1)).any(axis=1).sum() >= wl.T // 4
+        assert oracle.min_selection_gap(c.logits, b, wl.k).min() >= cases.GAP
+        np.testing.assert_allclose(c.w.sum(1), wl.scale, rtol=1e-12)

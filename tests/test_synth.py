@@ -50,3 +50,10 @@ def test_zipf_bias_prefers_low_ranks():
     assert b.shape == (512, 64) and b.dtype == np.float32
     col = b.mean(axis=0)
     assert col.max() - col.min() > 1.0
+
+
+def test_selection_bias_rows():
+    b = synth.selection_bias(0, 64)
+    m = synth.selection_bias(0, 64, 16)
+    assert b.shape == (64,) and m.shape == (16, 64) and b.dtype == m.dtype == np.float32
+    assert 0.05 < b.std() < 0.2 and not np.array_equal(m[0], b)
