@@ -90,6 +90,16 @@ typedef struct {
  * takes the logit reading. */
 #define MOE_FLAG_SELECTION_BIAS 1u
 
+/* Deterministic combine [PocketLLM, "Xing4.0-29B-A4B: the design record",
+ * section 4: float atomics make the top-k sum differ from run to run].
+ * Batches above 8 tokens then store each route's weighted down output once
+ * (no atomics) and add a token's routes in slot order, the shared expert
+ * last, so equal inputs give equal output bits on every call.  It costs an
+ * extra [routes][H] fp32 buffer (max_tokens * (top_k + n_shared) rows,
+ * allocated at create) and one write and one read of it per call.  Batches
+ * of up to 8 tokens are deterministic with or without the flag. */
+#define MOE_FLAG_DETERMINISTIC 2u
+
 /* Expert weights in IQ4_NL blocks (18 bytes each, no alignment needed).
  *   up, gate: [E][F][H/32] blocks     down: [E][H][F/32] blocks
  *   sh_up, sh_gate: [F][H/32]         sh_down: [H][F/32]  (NULL if no shared)
@@ -141,9 +151,11 @@ moe_status moe_route(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_
  *   weights  [T][k] fp32, any values; 4-byte aligned
  *   out      [T][H], MOE_DT_BF16 or MOE_DT_FP32, 16-byte aligned; the sum is
  *            formed in fp32 and rounded once (bf16: nearest-even)
- * The routed sum and the shared expert are accumulated in fp32 in any order
- * (fp32 additions of up to k+1 terms per element; not bit-reproducible
- * between runs). */
+ * The routed sum and the shared expert are accumulated in fp32.  Above 8
+ * tokens the order of those additions is whatever order the atomics commit
+ * in (up to k+1 terms per element), so outputs may differ in the last bits
+ * between runs, unless the layer was created with MOE_FLAG_DETERMINISTIC;
+ * up to 8 tokens every addition has a fixed order. */
 moe_status moe_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
                        const int32_t *ids, const float *weights, void *out,
                        moe_dtype out_dtype, void *stream);

@@ -19,6 +19,7 @@ MOE_OK = 0
 MOE_DT_BF16 = 0
 MOE_DT_FP32 = 1
 MOE_FLAG_SELECTION_BIAS = 1  # the bias ranks experts only (noaux_tc); weights stay unbiased
+MOE_FLAG_DETERMINISTIC = 2   # slot-ordered combine: equal inputs give equal output bits
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_OUT_OF_MEMORY", 5: "MOE_ERR_CUDA",

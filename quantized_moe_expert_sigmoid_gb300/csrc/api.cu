@@ -73,7 +73,7 @@ void free_layer(Layer *L) {
   if (!L) return;
   void *ptrs[] = {L->gu, L->dn, L->logits, L->offsets, L->active, L->route_token,
                   L->route_weight, L->h32, L->out_acc, L->err, L->sync, L->x16, L->h16,
-                  L->tiles_ug, L->tiles_dn, L->tile_counts};
+                  L->tiles_ug, L->tiles_dn, L->tile_counts, L->ybuf, L->route_pos};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   if (L->tev) {
@@ -158,10 +158,14 @@ moe_status forward_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const
     }
     return MOE_OK;
   }
-  MOE_CUDA(cudaMemsetAsync(L->out_acc, 0, sizeof(float) * (size_t)T * L->H, st), "clear accumulator");
+  if (!L->deterministic)
+    MOE_CUDA(cudaMemsetAsync(L->out_acc, 0, sizeof(float) * (size_t)T * L->H, st), "clear accumulator");
   MOE_CUDA(moe::launch_route_plan(*L, ids, w, T, st), "route plan");
   MOE_CUDA(moe::launch_prefill_tc(*L, x, xdt, T, st, ev ? ev + 1 : nullptr), "tensor-core expert GEMMs");
-  MOE_CUDA(moe::launch_finalize(*L, T, out, odt, st), "finalize");
+  if (L->deterministic)
+    MOE_CUDA(moe::launch_combine_ordered(*L, T, out, odt, st), "ordered combine");
+  else
+    MOE_CUDA(moe::launch_finalize(*L, T, out, odt, st), "finalize");
   if (ev) MOE_CUDA(rec(ev[4], st), "timing event");
   return MOE_OK;
 }
@@ -203,7 +207,8 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   if (S != 0 && S != 1) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "n_shared = %d: need 0 or 1", S);
   if (!(sh->routed_scaling > 0.f)) return fail(MOE_ERR_INVALID_ARG, "routed_scaling must be > 0");
   if (sh->max_tokens < 1 || sh->max_tokens > 65536) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "max_tokens = %d: need 1..65536", sh->max_tokens);
-  if (sh->flags & ~MOE_FLAG_SELECTION_BIAS) return fail(MOE_ERR_INVALID_ARG, "flags = 0x%x: unknown bits", sh->flags);
+  if (sh->flags & ~(MOE_FLAG_SELECTION_BIAS | MOE_FLAG_DETERMINISTIC))
+    return fail(MOE_ERR_INVALID_ARG, "flags = 0x%x: unknown bits", sh->flags);
   if (!wt->up || !wt->gate || !wt->down) return fail(MOE_ERR_INVALID_ARG, "up, gate and down must be non-NULL");
   if (S && (!wt->sh_up || !wt->sh_gate || !wt->sh_down)) return fail(MOE_ERR_INVALID_ARG, "shared expert weights must be non-NULL when n_shared = 1");
   const void *wps[] = {wt->up, wt->gate, wt->down, S ? wt->sh_up : wt->up,
@@ -216,6 +221,7 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   L->H = H; L->E = E; L->k = k; L->F = F; L->S = S;
   L->scale = sh->routed_scaling;
   L->sel_bias = (sh->flags & MOE_FLAG_SELECTION_BIAS) ? 1 : 0;
+  L->deterministic = (sh->flags & MOE_FLAG_DETERMINISTIC) ? 1 : 0;
   L->max_tokens = sh->max_tokens;
   L->Hp = (int)round_up(H, moe::kSBW);
   L->Fp = (int)round_up(F, moe::kSBW);
@@ -242,7 +248,7 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   ALLOC(L->active, sizeof(int) * (E + S + 1));
   ALLOC(L->route_token, sizeof(int) * (int64_t)L->max_routes);
   ALLOC(L->route_weight, sizeof(float) * (int64_t)L->max_routes);
-  ALLOC(L->h32, sizeof(float) * (int64_t)L->max_routes * L->Fp);
+  ALLOC(L->h32, sizeof(float) * (int64_t)std::min(sh->max_tokens, moe::kFusedMaxTokens) * (k + S) * L->Fp);
   ALLOC(L->out_acc, sizeof(float) * (int64_t)sh->max_tokens * H);
   ALLOC(L->err, sizeof(unsigned));
   ALLOC(L->sync, 4 * sizeof(unsigned));
@@ -253,6 +259,10 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   ALLOC(L->tiles_ug, sizeof(moe::TcTile) * (int64_t)moe::tc_max_tiles(*L, true));
   ALLOC(L->tiles_dn, sizeof(moe::TcTile) * (int64_t)moe::tc_max_tiles(*L, false));
   ALLOC(L->tile_counts, 2 * sizeof(int));
+  if (L->deterministic) {
+    ALLOC(L->ybuf, sizeof(float) * (int64_t)L->max_routes * L->Hp);
+    ALLOC(L->route_pos, sizeof(int) * (int64_t)sh->max_tokens * k);
+  }
 #undef ALLOC
 
   cudaError_t e = cudaSuccess;

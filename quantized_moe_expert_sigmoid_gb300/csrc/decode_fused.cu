@@ -116,7 +116,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
   __shared__ int sel_id[kFusedMaxTokens][8];
   __shared__ float sel_w[kFusedMaxTokens][8];
   __shared__ float red[kConsumerWarps][TT];
-  __shared__ float rowacc[kMaxRowsCta][TT];
 
   const Layer &L = p.L;
   const int T = p.T, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -641,7 +640,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
       for (int m = 0; m < kUnits; ++m)
 #pragma unroll
         for (int t = 0; t < TT; ++t) acc[m][t] = 0.f;
-      for (int idx = ct; idx < kMaxRowsCta * TT; idx += kConsumers) (&rowacc[0][0])[idx] = 0.f;
       int grp_end = -1, grp_rs = 0;  // experts [.., grp_end) have their h in hq
       for (; i < n_items; ++i) {
         const Item it = items[i];
@@ -755,27 +753,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
       }
-      // ---- reduce the units of each row and write the owned output rows ----
+      // ---- reduce the units of each row in a fixed order and write the
+      // owned output rows.  A row's npd units are consecutive in u, so each
+      // group of g lanes (g = 32, or 16 when npd is an odd multiple of 16)
+      // holds part of one row; the group sums go to the ring, idle once
+      // every consumer is past its last stage, and are added in group order.
+      named_sync(kBarConsumers, kConsumers);
+      float *part = reinterpret_cast<float *>(ring);  // [units / g][TT]
+      const int g = (npd & 31) == 0 ? 32 : 16;
 #pragma unroll
       for (int m = 0; m < kUnits; ++m) {
         const int u = ct + kConsumers * m;
-        const int rr = u / npd;
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
           if (t < T) {
-            if ((npd & 31) == 0) {  // a warp's 32 units lie in one row
-              const float v = warp_sum(acc[m][t]);
-              if (lane == 0 && rr < nrows) atomicAdd(&rowacc[rr][t], v);
-            } else if (rr < nrows) {
-              atomicAdd(&rowacc[rr][t], acc[m][t]);
-            }
+            float v = acc[m][t];
+            if (g == 32) v += __shfl_xor_sync(0xffffffffu, v, 16);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            if ((lane & (g - 1)) == 0 && u / npd < nrows) part[(u / g) * TT + t] = v;
           }
         }
       }
       named_sync(kBarConsumers, kConsumers);
+      const int gpr = npd / g;  // groups per row
       for (int idx = ct; idx < nrows * T; idx += kConsumers) {
         const int t = idx / nrows, rr = idx % nrows;
-        const float v = rowacc[rr][t];
+        float v = part[(rr * gpr) * TT + t];
+        for (int j = 1; j < gpr; ++j) v += part[(rr * gpr + j) * TT + t];
         const int64_t o = (int64_t)t * H + n0 + rr;
         if (p.out_bf16)
           reinterpret_cast<__nv_bfloat16 *>(p.out)[o] = __float2bfloat16_rn(v);

@@ -53,6 +53,7 @@ struct Layer {
   int H, E, k, F, S;  // S = number of shared experts (0 or 1)
   float scale;
   int sel_bias;              // 1: the bias shifts expert selection only (MOE_FLAG_SELECTION_BIAS)
+  int deterministic;         // 1: slot-ordered combine, no float atomics (MOE_FLAG_DETERMINISTIC)
   int max_tokens;
   int Hp, Fp;                // H and F padded to multiples of 256
   int64_t gu_row_bytes;      // Hp/256 * 144
@@ -72,8 +73,11 @@ struct Layer {
   int *active = nullptr;     // [E+S+1] ids of experts with routes; [E+S] = count
   int *route_token = nullptr;   // [max_routes]
   float *route_weight = nullptr; // [max_routes]
-  float *h32 = nullptr;      // [max_routes][Fp] SwiGLU output (fp32)
+  float *h32 = nullptr;      // [min(max_tokens, 8) * (k+S)][Fp] SwiGLU output of the decode kernel
   float *out_acc = nullptr;  // [max_tokens][H] fp32 accumulator
+  // deterministic combine only (else nullptr)
+  float *ybuf = nullptr;     // [max_routes][Hp] weighted down outputs, route order
+  int *route_pos = nullptr;  // [max_tokens*k] position of route t*k+j in route order, -1: dropped
   unsigned *err = nullptr;   // sticky device error word
   unsigned *sync = nullptr;  // [4] arrival counters of the single-launch decode kernel
 
@@ -126,12 +130,13 @@ cudaError_t launch_router_topk(const Layer &L, const float *logits, int parts, c
 cudaError_t launch_route_plan(const Layer &L, const int32_t *ids, const float *weights,
                               int T, cudaStream_t stream);
 
-// expert_simt.cu: CUDA-core expert path (any T).
-cudaError_t launch_upgate_simt(const Layer &L, const void *x, moe_dtype xdt, int T,
-                               cudaStream_t stream);
-cudaError_t launch_down_simt(const Layer &L, int T, cudaStream_t stream);
+// combine.cu: the output of the batched path.  finalize: out = round(out_acc);
+// ordered: out[t] = sum over slots j in order of ybuf[route_pos[t*k+j]], then
+// + ybuf[offsets[E] + t] (shared), rounded once.
 cudaError_t launch_finalize(const Layer &L, int T, void *out, moe_dtype odt,
                             cudaStream_t stream);
+cudaError_t launch_combine_ordered(const Layer &L, int T, void *out, moe_dtype odt,
+                                   cudaStream_t stream);
 
 // decode_fused.cu: the whole layer in one launch for T <= kFusedMaxTokens.
 // ids_in == nullptr: route inside (router_w, bias used; ids_out/w_out

@@ -8,6 +8,8 @@
 // Route r = t*k + j (token t, slot j).  The permutation orders routes by
 // (expert, t, j): within an expert, routes keep their original order.  The
 // shared expert is segment E and holds every token in order, weight 1.
+// For the deterministic combine the kernel also writes route_pos[r], the
+// position route r was given (-1 for a dropped route).
 //
 // One CTA of 1024 threads (32 warps).  Warp w owns a contiguous run of
 // routes and walks it 32 at a time: lanes with the same expert find each
@@ -47,7 +49,7 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(
     int *__restrict__ offsets, int *__restrict__ active, int *__restrict__ route_token,
     float *__restrict__ route_weight, unsigned *__restrict__ err, TcTile *__restrict__ ug,
     TcTile *__restrict__ dn, int *__restrict__ tile_counts, int ug_mtiles, int dn_mtiles, int max_ug,
-    int max_dn) {
+    int max_dn, int *__restrict__ route_pos) {
   __shared__ int cnt[32 * kMaxE];  // [warp][expert] counts, then bases
   __shared__ int off[kMaxE + 2];
   __shared__ int act[kMaxE + 2];
@@ -156,11 +158,13 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(
       const int e = ev[i];
       const bool ok = e >= 0 && e < E;
       const unsigned peers = same_expert_lanes(e, ok);
+      int pos = -1;  // dropped (invalid id)
       if (ok) {
-        const int pos = off[e] + cnt[warp * E + e] + __popc(peers & lt_mask);
+        pos = off[e] + cnt[warp * E + e] + __popc(peers & lt_mask);
         route_token[pos] = r / k;
         route_weight[pos] = wv[i];
       }
+      if (route_pos && r < r_end) route_pos[r] = pos;
       __syncwarp();
       if (ok && (peers & lt_mask) == 0) cnt[warp * E + e] += __popc(peers);
       __syncwarp();
@@ -207,7 +211,8 @@ cudaError_t launch_route_plan(const Layer &L, const int32_t *ids, const float *w
   route_plan_kernel<<<1, 1024, 0, stream>>>(ids, weights, T, L.k, L.E, L.S, L.offsets, L.active,
                                             L.route_token, L.route_weight, L.err, L.tiles_ug,
                                             L.tiles_dn, L.tile_counts, L.Fp / 128, L.Hp / 256,
-                                            tc_max_tiles(L, true), tc_max_tiles(L, false));
+                                            tc_max_tiles(L, true), tc_max_tiles(L, false),
+                                            L.deterministic ? L.route_pos : nullptr);
   count_launches(1);
   return cudaGetLastError();
 }

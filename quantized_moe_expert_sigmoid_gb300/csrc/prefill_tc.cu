@@ -11,8 +11,9 @@
 //              accumulators; h = silu(G) * U -> fp16
 //   down       per tile (expert, 256 hidden rows, <= 256 routes): two
 //              M = 128 MMAs on one h tile; out_acc[token][row] +=
-//              route weight * Y (fp32)
-//   finalize   out = round(out_acc)
+//              route weight * Y (fp32), or with the deterministic combine
+//              ybuf[route][row] = route weight * Y, one writer per element
+//   finalize   out = round(out_acc), or the slot-ordered sum of ybuf
 // Operands are fp16 (kind::f16, fp32 accumulate): the IQ4_NL codes are
 // integers |c| <= 127, exact in fp16, and the per-block scale is applied when
 // a tile is dequantised (one rounding of d * code); bf16 weights and h would
@@ -96,6 +97,7 @@ struct TcParams {
   const float *route_weight;
   __half *h16;       // up/gate output [routes][Fp]
   float *out_acc;    // down output accumulator [T][H]
+  float *ybuf;       // nullptr, or per-route down outputs [routes][Hp] (deterministic combine)
   unsigned *err;
   int H, Hp, Fp;
 };
@@ -350,9 +352,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
               const int col = c0 + j;
               if (col < t.count) {
                 const float wgt = ep_w[col];
-                float *orow = p.out_acc + (int64_t)ep_tok[col] * p.H;
-                if (n0 < p.H) atomicAdd(orow + n0, wgt * __uint_as_float(g[j]));
-                if (n1 < p.H) atomicAdd(orow + n1, wgt * __uint_as_float(u[j]));
+                if (p.ybuf) {  // one writer per element; the combine adds in slot order
+                  float *yrow = p.ybuf + (int64_t)(t.row0 + col) * p.Hp;
+                  if (n0 < p.H) yrow[n0] = wgt * __uint_as_float(g[j]);
+                  if (n1 < p.H) yrow[n1] = wgt * __uint_as_float(u[j]);
+                } else {
+                  float *orow = p.out_acc + (int64_t)ep_tok[col] * p.H;
+                  if (n0 < p.H) atomicAdd(orow + n0, wgt * __uint_as_float(g[j]));
+                  if (n1 < p.H) atomicAdd(orow + n1, wgt * __uint_as_float(u[j]));
+                }
               }
             }
           }
@@ -519,6 +527,7 @@ cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int 
   p.route_weight = L.route_weight;
   p.h16 = L.h16;
   p.out_acc = L.out_acc;
+  p.ybuf = L.deterministic ? L.ybuf : nullptr;
   p.err = L.err;
   p.H = L.H;
   p.Hp = L.Hp;

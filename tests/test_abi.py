@@ -68,7 +68,7 @@ def _create(lib, **over):
     (dict(hidden=250), 2), (dict(hidden=0), 2), (dict(expert_ffn=48 + 1), 2),
     (dict(n_experts=0), 2), (dict(n_experts=300), 2), (dict(top_k=9), 2),
     (dict(top_k=9, n_experts=8), 2), (dict(n_shared=2), 2), (dict(max_tokens=0), 2),
-    (dict(routed_scaling=0.0), 1), (dict(flags=2), 1), (dict(flags=0x80000001), 1), ({}, 1)])
+    (dict(routed_scaling=0.0), 1), (dict(flags=4), 1), (dict(flags=0x80000001), 1), ({}, 1)])
 def test_create_validates_before_touching_the_gpu(lib, over, status):
     st, handle = _create(lib, **over)
     assert st == status, moe.moe_last_error()
@@ -78,9 +78,10 @@ def test_create_validates_before_touching_the_gpu(lib, over, status):
         assert "flags" in moe.moe_last_error()
 
 
-def test_selection_bias_flag_is_accepted(lib):
-    # a known flag passes the flags check and fails later, on the NULL weights
-    st, handle = _create(lib, flags=moe.MOE_FLAG_SELECTION_BIAS)
+@pytest.mark.parametrize("flags", [1, 2, 3])
+def test_known_flags_are_accepted(lib, flags):
+    # known flags pass the flags check and fail later, on the NULL weights
+    st, handle = _create(lib, flags=flags)
     assert st == 1 and handle is None
     assert "flags" not in moe.moe_last_error()
 
@@ -111,5 +112,6 @@ def test_stage_timing_argument_checks(lib):
 
 def test_flag_constants_match_the_header():
     src = (pathlib.Path(__file__).resolve().parents[1] / "include" / "moe_gb300.h").read_text()
-    m = re.search(r"#define\s+MOE_FLAG_SELECTION_BIAS\s+(\d+)u", src)
-    assert m and int(m.group(1)) == moe.MOE_FLAG_SELECTION_BIAS
+    for name in ("MOE_FLAG_SELECTION_BIAS", "MOE_FLAG_DETERMINISTIC"):
+        m = re.search(r"#define\s+%s\s+(\d+)u" % name, src)
+        assert m and int(m.group(1)) == getattr(moe, name), name

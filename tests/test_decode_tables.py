@@ -73,11 +73,3 @@ def test_relabel_pairs_share_a_sign():
     for j in range(8):
         a, b = CODEBOOK[2 * j], CODEBOOK[2 * j + 1]
         assert (a < 0) == (b < 0)
-
-
-def test_cuda_core_table_is_in_label_order():
-    src = open(os.path.join(CSRC, "expert_simt.cu")).read()
-    body = re.search(r"c_codebook\[16\] = \{([^}]*)\}", src).group(1)
-    table = [float(v.strip().rstrip("f")) for v in body.split(",")]
-    for i, v in enumerate(CODEBOOK):
-        assert table[_label(i)] == v
