@@ -33,8 +33,10 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-EXPERT_BYTES = 6_193_152           # 3 IQ4_NL matrices of 2,064,384 B
-H, E, K, F = 3584, 64, 4, 1024
+def expert_bytes_of(wl):
+    """IQ4_NL bytes of one expert: up, gate and down, 18 bytes per 32 weights
+    (6,193,152 B for the Xing4 layer)."""
+    return 3 * wl.F * (wl.H // 32) * 18
 
 
 def parse():
@@ -44,7 +46,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=64)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="decode1",
-                   choices=["decode1", "decode64", "prefill4096", "trunk38_t1", "trunk38_t16"])
+                   choices=["decode1", "decode64", "prefill4096", "trunk38_t1", "trunk38_t16",
+                            "k2h_decode1", "k2h_decode64", "k2h_prefill1024"])
     p.add_argument("--layers", type=int, default=16, help="resident layers the steps rotate over")
     p.add_argument("--graph-steps", type=int, default=32)
     p.add_argument("--e2e-steps", type=int, default=2000)
@@ -72,7 +75,8 @@ def bench_config(args, wl, world):
             "workload": wl.name, "tokens_per_step": T, "layers": wl.n_layers, "hidden": wl.H,
             "experts": wl.E, "top_k": wl.k, "expert_ffn": wl.F, "shared_experts": 1,
             "parallelism": f"replicas x{world}",
-            "l2": f"{wl.n_layers} resident layers ({wl.n_layers * 403.5 / 1000:.1f} GB of weights, "
+            "l2": f"{wl.n_layers} resident layers "
+                  f"({wl.n_layers * ((wl.E + 1) * expert_bytes_of(wl) + wl.E * wl.H * 4) / 1e9:.1f} GB of weights, "
                   "far larger than L2), 16 rotating inputs",
             "graph_steps": G}
     NL = args.layers if T < 64 else max(1, min(args.layers, 2))
@@ -80,7 +84,7 @@ def bench_config(args, wl, world):
     G = max(1, min(args.graph_steps, args.steps))
     return NL, NX, G, {
         "workload": wl.name, "tokens_per_step": T, "hidden": wl.H, "experts": wl.E,
-        "top_k": wl.k, "expert_ffn": wl.F, "shared_experts": 1,
+        "top_k": wl.k, "expert_ffn": wl.F, "shared_experts": 1, "routed_scaling": wl.scale,
         "parallelism": f"replicas x{world}",
         "l2": f"rotating over {NL} resident layers and {NX} inputs (inputs larger than L2)",
         "graph_steps": G}
@@ -100,10 +104,10 @@ def replay_percentiles(start, marks, per_replay_steps):
     return {"p10": pick(0.1), "median": pick(0.5), "p90": pick(0.9), "replays": len(ts)}
 
 
-def algorithmic_bytes(T, distinct_experts):
+def algorithmic_bytes(wl, T, distinct_experts):
     """HBM bytes one call must move at least: the selected experts' and the
     shared expert's IQ4_NL weights, the fp32 router, x in and out (bf16)."""
-    return (distinct_experts + 1) * EXPERT_BYTES + E * H * 4 + 2 * T * H * 2
+    return (distinct_experts + 1) * expert_bytes_of(wl) + wl.E * wl.H * 4 + 2 * T * wl.H * 2
 
 
 class Clocks:
@@ -316,8 +320,8 @@ def run_ours(args, rank, world, local_rank):
     for s in range(min(G, steps)):
         distinct.append(len(set(ids[s].flatten().tolist())))
     mean_distinct = sum(distinct) / len(distinct)
-    alg_bytes = algorithmic_bytes(T, mean_distinct)
-    expert_bytes = (mean_distinct + 1) * EXPERT_BYTES
+    alg_bytes = algorithmic_bytes(wl, T, mean_distinct)
+    expert_bytes = (mean_distinct + 1) * expert_bytes_of(wl)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -383,7 +387,7 @@ def run_ours(args, rank, world, local_rank):
         "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in/out, IQ4_NL weights, fp32 accumulate",
-        "data": "synthetic (seeded; random IQ4_NL weights of the Xing4 layer shapes)",
+        "data": "synthetic (seeded; random IQ4_NL weights of the workload's layer shapes)",
         "config": cfg,
         "us_per_layer": ms_per_step * 1e3,
         "expert_weight_gbs": expert_bytes / (ms_per_step * 1e-3) / 1e9,
@@ -482,7 +486,7 @@ def run_trunk(args, rank, world, local_rank):
     ms_per_step = ms / steps
     # bytes of the last step: every layer's selected experts + shared, routers, activations
     distinct = [len(set(trunk.ids[l][:T].flatten().tolist())) for l in range(NL)]
-    expert_bytes = sum(d + 1 for d in distinct) * EXPERT_BYTES
+    expert_bytes = sum(d + 1 for d in distinct) * expert_bytes_of(wl)
     alg_bytes = expert_bytes + NL * (wl.E * wl.H * 4 + T * wl.H * (2 + 4 + 4 + 4 + 2))
 
     e2e = None

@@ -263,6 +263,16 @@ WORKLOADS = {
     "prefill4096": Workload("Xing4 MoE layer, prefill 4,096 tokens, Zipf-skewed routing", 3584, 64, 4, 1024, 4096, "bf16", 0.02, zipf=True),
     "trunk38_t1": Workload("38-layer Xing4 MoE trunk, batch 1", 3584, 64, 4, 1024, 1, "bf16", 0.02, n_layers=38),
     "trunk38_t16": Workload("38-layer Xing4 MoE trunk, batch 16", 3584, 64, 4, 1024, 16, "bf16", 0.02, n_layers=38),
+    # the K2-Horizon FFN router: 8 of 100 routed experts + 1 shared, weights
+    # normalised and scaled by 2.5, hidden 2,560.  The expert width is not
+    # given: 10.00 GiB for 4,500 expert groups at IQ3_XS's ~3.3 bits per
+    # weight is ~5.8 M weights = 3 x 2,560 x ~750 per expert; 768 is taken.
+    "k2h_decode1": Workload("K2-Horizon-shaped MoE layer, decode batch 1 (H2560 E100 top-8 F768, x2.5)",
+                            2560, 100, 8, 768, 1, "bf16", 0.024, scale=2.5),
+    "k2h_decode64": Workload("K2-Horizon-shaped MoE layer, batched decode 64 tokens",
+                             2560, 100, 8, 768, 64, "bf16", 0.024, scale=2.5),
+    "k2h_prefill1024": Workload("K2-Horizon-shaped MoE layer, prefill 1,024 tokens",
+                                2560, 100, 8, 768, 1024, "bf16", 0.024, scale=2.5),
 }
 
 
