@@ -160,6 +160,18 @@ moe_status moe_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype, int3
                        const int32_t *ids, const float *weights, void *out,
                        moe_dtype out_dtype, void *stream);
 
+/* Dense FFN block: out[t] = W_down (silu(W_gate x[t]) * (W_up x[t])) for
+ * every token, no router and no weight [PocketLLM, "Xing4.0-29B-A4B: the
+ * design record", section 1: the first two of the forty blocks are dense
+ * (first_k_dense_replace = 2); EPQ, "模型與路由": dense FFN width 9,216].
+ * The block is a layer created with n_experts = 1, top_k = 1, n_shared = 0
+ * (routed_scaling is not used) holding the FFN as expert 0; this call runs
+ * it on the same kernels as moe_forward with every token routed to expert 0
+ * at weight 1.  Arguments and errors as for moe_forward; a layer of any
+ * other shape returns MOE_ERR_INVALID_ARG. */
+moe_status moe_dense_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
+                             void *out, moe_dtype out_dtype, void *stream);
+
 /* moe_route followed by moe_forward on the same stream, with the same
  * arguments; ids and weights are written as by moe_route.  For small T the
  * two run fused in as few launches as the layer allows. */

@@ -230,6 +230,17 @@ def rmsnorm(r: np.ndarray, eps: float) -> np.ndarray:
     return u
 
 
+def dense_ffn(x: np.ndarray, ew) -> np.ndarray:
+    """Dense FFN block [PocketLLM "Xing4.0-29B-A4B: the design record",
+    section 1: the first two blocks are dense]: out[t] = W_down (silu(W_gate
+    x[t]) * (W_up x[t])) with ew holding one expert (up/gate/down [1, ...])
+    and no shared expert -- the layer forward with every token routed to
+    expert 0 at weight 1."""
+    assert ew.up.shape[0] == 1 and getattr(ew, "sh_up", None) is None
+    T = np.asarray(x).shape[0]
+    return moe_forward(x, np.zeros((T, 1), np.int32), np.ones((T, 1)), ew)
+
+
 def min_topk_gap(logits: np.ndarray, k: int) -> np.ndarray:
     """Per token, the smallest gap between adjacent sigmoid scores among the
     k+1 largest (fp64).  The routing of a token is unambiguous when it is

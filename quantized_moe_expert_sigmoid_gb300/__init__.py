@@ -29,7 +29,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 EXPORTS = ["moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
            "moe_layer_forward_routed", "moe_residual_rmsnorm", "moe_layer_check",
            "moe_layer_weight_bytes", "moe_launch_count", "moe_status_string", "moe_last_error",
-           "moe_route_noalloc"]
+           "moe_route_noalloc", "moe_dense_forward"]
 
 
 class MoeError(RuntimeError):
@@ -73,6 +73,7 @@ def load_library(path: str | None = None):
     lib.moe_layer_destroy.argtypes = [P]
     lib.moe_route.argtypes = [P, P, I32, I32, P, P, I64, P, P, P]
     lib.moe_forward.argtypes = [P, P, I32, I32, P, P, P, I32, P]
+    lib.moe_dense_forward.argtypes = [P, P, I32, I32, P, I32, P]
     lib.moe_layer_forward_routed.argtypes = [P, P, I32, I32, P, P, I64, P, P, P, I32, P]
     lib.moe_residual_rmsnorm.argtypes = [P, P, I32, P, I32, I32, F, P]
     lib.moe_layer_check.argtypes = [P]
@@ -90,7 +91,7 @@ def load_library(path: str | None = None):
     lib.moe_layer_stage_times.argtypes = [P, P, I32, ctypes.POINTER(I32)]
     for n in ("moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
               "moe_layer_forward_routed", "moe_residual_rmsnorm", "moe_layer_check",
-              "moe_layer_enable_timing", "moe_layer_stage_times"):
+              "moe_layer_enable_timing", "moe_layer_stage_times", "moe_dense_forward"):
         getattr(lib, n).restype = I32
     _lib = lib
     return lib
@@ -181,6 +182,13 @@ def moe_forward(layer, x, ids, weights, out, stream=None):
                                       x.shape[0], _ptr(ids, "ids", d["i32"]),
                                       _ptr(weights, "weights", d["f32"]), _ptr(out, "out", d["x"]),
                                       _dtype(out), _stream(stream)))
+
+
+def moe_dense_forward(layer, x, out, stream=None):
+    d = _dt()
+    _check(load_library().moe_dense_forward(ctypes.c_void_p(layer), _ptr(x, "x", d["x"]), _dtype(x),
+                                            x.shape[0], _ptr(out, "out", d["x"]), _dtype(out),
+                                            _stream(stream)))
 
 
 def moe_layer_forward_routed(layer, x, router_w, ids, weights, out, logit_bias=None,
@@ -311,6 +319,13 @@ class MoeLayer:
         import torch
         out = torch.empty((x.shape[0], self.H), dtype=out_dtype or x.dtype, device=x.device)
         moe_forward(self.handle, x, ids, weights, out, stream=stream)
+        return out
+
+    def dense_forward(self, x, out_dtype=None, stream=None):
+        """The FFN of a dense block (a layer of one expert, top-1) on every token."""
+        import torch
+        out = torch.empty((x.shape[0], self.H), dtype=out_dtype or x.dtype, device=x.device)
+        moe_dense_forward(self.handle, x, out, stream=stream)
         return out
 
     def forward_routed(self, x, router_w, logit_bias=None, out_dtype=None, stream=None):

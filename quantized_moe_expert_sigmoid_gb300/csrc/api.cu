@@ -73,7 +73,8 @@ void free_layer(Layer *L) {
   if (!L) return;
   void *ptrs[] = {L->gu, L->dn, L->logits, L->offsets, L->active, L->route_token,
                   L->route_weight, L->h32, L->out_acc, L->err, L->sync, L->x16, L->h16,
-                  L->tiles_ug, L->tiles_dn, L->tile_counts, L->ybuf, L->route_pos};
+                  L->tiles_ug, L->tiles_dn, L->tile_counts, L->ybuf, L->route_pos,
+                  L->dense_ids, L->dense_w};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   if (L->tev) {
@@ -259,6 +260,10 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   ALLOC(L->tiles_ug, sizeof(moe::TcTile) * (int64_t)moe::tc_max_tiles(*L, true));
   ALLOC(L->tiles_dn, sizeof(moe::TcTile) * (int64_t)moe::tc_max_tiles(*L, false));
   ALLOC(L->tile_counts, 2 * sizeof(int));
+  if (E == 1 && k == 1) {
+    ALLOC(L->dense_ids, sizeof(int32_t) * (int64_t)sh->max_tokens);
+    ALLOC(L->dense_w, sizeof(float) * (int64_t)sh->max_tokens);
+  }
   if (L->deterministic) {
     ALLOC(L->ybuf, sizeof(float) * (int64_t)L->max_routes * L->Hp);
     ALLOC(L->route_pos, sizeof(int) * (int64_t)sh->max_tokens * k);
@@ -269,6 +274,10 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   if (e == cudaSuccess) e = cudaMemsetAsync(L->gu, 0, (size_t)gu_total, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(L->dn, 0, (size_t)dn_total, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(L->err, 0, sizeof(unsigned), st);
+  if (e == cudaSuccess && L->dense_ids) {
+    e = cudaMemsetAsync(L->dense_ids, 0, sizeof(int32_t) * (size_t)sh->max_tokens, st);
+    if (e == cudaSuccess) e = moe::launch_fill(L->dense_w, 1.0f, sh->max_tokens, st);
+  }
   if (e == cudaSuccess) e = cudaMemsetAsync(L->sync, 0, 4 * sizeof(unsigned), st);
   const int64_t up_bytes = (int64_t)F * (H / 32) * 18;
   const int64_t dn_bytes = (int64_t)H * (F / 32) * 18;
@@ -314,6 +323,20 @@ moe_status moe_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype, int3
   Layer *L = reinterpret_cast<Layer *>(layer);
   cudaEvent_t *ev = (L && T > 0) ? timing_slot(L) : nullptr;
   moe_status r = forward_impl(L, x, x_dtype, T, ids, weights, out, out_dtype, (cudaStream_t)stream, ev);
+  if (r == MOE_OK && ev) timing_advance(L);
+  return r;
+}
+
+moe_status moe_dense_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
+                             void *out, moe_dtype out_dtype, void *stream) {
+  Layer *L = reinterpret_cast<Layer *>(layer);
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+  if (!L->dense_ids)
+    return fail(MOE_ERR_INVALID_ARG, "moe_dense_forward needs a layer with n_experts = 1 and top_k = 1 (got %d, %d)",
+                L->E, L->k);
+  cudaEvent_t *ev = T > 0 ? timing_slot(L) : nullptr;
+  moe_status r = forward_impl(L, x, x_dtype, T, L->dense_ids, L->dense_w, out, out_dtype,
+                              (cudaStream_t)stream, ev);
   if (r == MOE_OK && ev) timing_advance(L);
   return r;
 }

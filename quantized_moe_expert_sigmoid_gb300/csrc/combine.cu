@@ -66,7 +66,19 @@ __global__ void combine_ordered_kernel(const float *__restrict__ ybuf, const int
   store4(out, i, acc, bf16);
 }
 
+__global__ void fill_kernel(float *__restrict__ dst, float v, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = v;
+}
+
 }  // namespace
+
+cudaError_t launch_fill(float *dst, float value, int n, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  fill_kernel<<<(n + 255) / 256, 256, 0, stream>>>(dst, value, n);
+  count_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_finalize(const Layer &L, int T, void *out, moe_dtype odt, cudaStream_t stream) {
   const int64_t n = (int64_t)T * L.H;

@@ -78,6 +78,9 @@ struct Layer {
   // deterministic combine only (else nullptr)
   float *ybuf = nullptr;     // [max_routes][Hp] weighted down outputs, route order
   int *route_pos = nullptr;  // [max_tokens*k] position of route t*k+j in route order, -1: dropped
+  // dense blocks (n_experts = 1, top_k = 1): every token to expert 0 at weight 1
+  int32_t *dense_ids = nullptr;  // [max_tokens] zeros
+  float *dense_w = nullptr;      // [max_tokens] ones
   unsigned *err = nullptr;   // sticky device error word
   unsigned *sync = nullptr;  // [4] arrival counters of the single-launch decode kernel
 
@@ -133,6 +136,7 @@ cudaError_t launch_route_plan(const Layer &L, const int32_t *ids, const float *w
 // combine.cu: the output of the batched path.  finalize: out = round(out_acc);
 // ordered: out[t] = sum over slots j in order of ybuf[route_pos[t*k+j]], then
 // + ybuf[offsets[E] + t] (shared), rounded once.
+cudaError_t launch_fill(float *dst, float value, int n, cudaStream_t stream);  // dst[0..n) = value
 cudaError_t launch_finalize(const Layer &L, int T, void *out, moe_dtype odt,
                             cudaStream_t stream);
 cudaError_t launch_combine_ordered(const Layer &L, int T, void *out, moe_dtype odt,

@@ -152,6 +152,15 @@ def expert_weights(seed: int, layer: int, E: int, H: int, F: int,
     return ExpertWeights(up, gate, down, s_up, s_gate, s_down)
 
 
+def dense_ffn_weights(seed: int, layer: int, H: int, F: int) -> ExpertWeights:
+    """A dense FFN block's IQ4_NL matrices as a one-expert layer with no
+    shared expert (streams of their own, distinct from any expert's)."""
+    up = iq4nl_blocks(seed, "dense/up", F, H, layer)[None]
+    gate = iq4nl_blocks(seed, "dense/gate", F, H, layer)[None]
+    down = iq4nl_blocks(seed, "dense/down", H, F, layer)[None]
+    return ExpertWeights(up, gate, down, None, None, None)
+
+
 def expert_subset_weights(seed: int, layer: int, experts, H: int, F: int,
                           n_shared: int = 1) -> ExpertWeights:
     """The matrices of the routed experts `experts` (in that order) of layer

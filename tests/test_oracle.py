@@ -302,12 +302,23 @@ def pin_selection_bias_zero_and_forcing():
         np.testing.assert_allclose(w2[t], 2.0 * sel / sel.sum(), rtol=1e-14)
 
 
+def pin_dense_block():
+    # a one-expert layer with weight 1 and no shared expert is the plain FFN,
+    # checked against the dense loop above
+    ew = synth.dense_ffn_weights(9, 0, 64, 96)
+    x = oracle.to_f64(synth.activations(9, "x", 4, 64, dtype="fp32"), "fp32")
+    out = oracle.dense_ffn(x, ew)
+    for t in range(x.shape[0]):
+        want = _dense_ffn(ew.up[0], ew.gate[0], ew.down[0], x[t])
+        assert np.allclose(out[t], want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
+
+
 PINS = [pin_fp16_values, pin_golden_blocks, pin_matrix_bytes, pin_roundtrip,
         pin_router_hand_case, pin_router_brute_force, pin_weights_sum_to_scale,
         pin_rank_one_closed_form, pin_all_experts_equals_dense, pin_top1_special_case,
         pin_permutation_and_token_independence, pin_zero_weight_route_contributes_nothing,
         pin_rmsnorm_closed_form, pin_invalid_ids_rejected, pin_selection_bias_hand_case,
-        pin_selection_bias_zero_and_forcing]
+        pin_selection_bias_zero_and_forcing, pin_dense_block]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
