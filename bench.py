@@ -46,7 +46,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=64)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="decode1",
-                   choices=["decode1", "decode64", "prefill4096", "trunk38_t1", "trunk38_t16",
+                   choices=["decode1", "decode8", "decode64", "prefill4096", "trunk38_t1", "trunk38_t16",
                             "k2h_decode1", "k2h_decode64", "k2h_prefill1024"])
     p.add_argument("--layers", type=int, default=16, help="resident layers the steps rotate over")
     p.add_argument("--graph-steps", type=int, default=32)

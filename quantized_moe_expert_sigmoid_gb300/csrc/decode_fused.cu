@@ -62,6 +62,8 @@ constexpr int kH4 = 4;     // float4 loads in flight per thread when gathering h
 constexpr uint32_t kPollLimit = 1u << 24;
 constexpr uint32_t kSpinLimit = 1u << 21;
 constexpr int kBarConsumers = 1;  // named barrier ids (0 is __syncthreads)
+constexpr int kBarPlan = 2;       // producer -> consumers: route plan written
+constexpr uint64_t kWaitNs = 500000000ull;  // 0.5 s per copy wait before giving up
 
 struct Params {
   Layer L;
@@ -105,7 +107,7 @@ __device__ __forceinline__ float load_x(const void *x, int bf16, int64_t i) {
 template <int TT, int NP, int NPD>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], wr_bar, plan_bar;
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], wr_bar;
   __shared__ Item items[kMaxItems];
   __shared__ int n_items, n_shared_items, n_ex, status;
   __shared__ int r_tok[kMaxSlots];
@@ -149,7 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
       mbar_init(&empty_bar[s], kConsumerWarps);
     }
     mbar_init(&wr_bar, 1);
-    mbar_init(&plan_bar, 1);
     fence_mbar_init();
     n_items = 0;
     n_ex = 0;
@@ -392,13 +393,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
       }
     }
     __syncwarp();
+    named_arrive(kBarPlan, kThreads);  // the tables above are visible to the consumers
     if (lane == 0) {
-      mbar_arrive(&plan_bar);  // release: the tables above become visible to the waiters
       int i = issued;
       for (; i < n_items && i < nst; ++i) issue(i);  // stages never used yet
       for (; i < n_items; ++i) {
         const int s = i % nst;
-        if (!mbar_wait_bounded(&empty_bar[s], (uint32_t)((i / nst) - 1) & 1u, kPollLimit)) {
+        if (!mbar_wait_suspend(&empty_bar[s], (uint32_t)((i / nst) - 1) & 1u, kWaitNs)) {
           atomicOr(&status, 2);
           break;
         }
@@ -528,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     auto process_upgate = [&](int i) {
       const Item it = items[i];
       const int s = i % nst;
-      if (!mbar_wait_sleep(&full_bar[s], (uint32_t)(i / nst) & 1u, kPollLimit, 32)) atomicOr(&status, 2);
+      if (!mbar_wait_suspend(&full_bar[s], (uint32_t)(i / nst) & 1u, kWaitNs)) atomicOr(&status, 2);
       const int rs = ex_rs[it.a], nr = ex_rs[it.a + 1] - rs;
       const int fl = warp % kGroupWarps;
       float accg[TT], accu[TT];
@@ -616,7 +617,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     const int my_group = warp / kGroupWarps;  // up/gate items rotate among the warp groups
     for (; i < n_shared_items; ++i)
       if (i % kItemGroups == my_group) process_upgate(i);
-    if (!mbar_wait_sleep(&plan_bar, 0, kPollLimit, 128)) atomicOr(&status, 2);
+    // the producer warp plans meanwhile; a hardware barrier (it arrives on
+    // every path) leaves it all the issue slots
+    named_sync(kBarPlan, kThreads);
     if (!(status & 1)) {
       for (; i < n_items && items[i].kind == 0; ++i)
         if (i % kItemGroups == my_group) process_upgate(i);
@@ -688,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         }
         const int hoff = rs - grp_rs;
         const int s = i % nst;
-        if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(i / nst) & 1u, kPollLimit)) atomicOr(&status, 2);
+        if (!mbar_wait_suspend(&full_bar[s], (uint32_t)(i / nst) & 1u, kWaitNs)) atomicOr(&status, 2);
         int rids[TT];
 #pragma unroll
         for (int t = 0; t < TT; ++t) rids[t] = t < T ? (int)rid[a][t] : -1;

@@ -107,6 +107,35 @@ __device__ __forceinline__ bool mbar_wait_ns(uint64_t *bar, uint32_t parity, uin
   }
 }
 
+// Wait for phase `parity` of `bar` with the thread suspended in hardware
+// between checks: each try_wait may suspend for up to `hint_ns` and returns
+// as soon as the phase completes, so waiting warps take no issue slots or
+// shared-memory bandwidth from the warps that compute.  Gives up (false)
+// after about `budget_ns` of wall time.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t *bar, uint32_t parity, uint64_t budget_ns) {
+  if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if (global_ns() - t0 > budget_ns) return false;
+  }
+}
+
+// Arrive on named barrier `id` without waiting (`n` threads take part).
+__device__ __forceinline__ void named_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // 1D bulk copy global -> shared, completing on `bar` (16-byte aligned
 // addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,

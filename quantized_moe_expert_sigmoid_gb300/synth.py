@@ -268,6 +268,7 @@ class Workload:
 WORKLOADS = {
     "tiny": Workload("tiny: H256 E8 top-2 F128, 4 tokens, fp32 x", 256, 8, 2, 128, 4, "fp32", 0.05),
     "decode1": Workload("Xing4 MoE layer, decode batch 1 (H3584 E64 top-4 F1024)", 3584, 64, 4, 1024, 1, "bf16", 0.02),
+    "decode8": Workload("Xing4 MoE layer, batched decode 8 tokens", 3584, 64, 4, 1024, 8, "bf16", 0.02),
     "decode64": Workload("Xing4 MoE layer, batched decode 64 tokens", 3584, 64, 4, 1024, 64, "bf16", 0.02),
     "prefill4096": Workload("Xing4 MoE layer, prefill 4,096 tokens, Zipf-skewed routing", 3584, 64, 4, 1024, 4096, "bf16", 0.02, zipf=True),
     "trunk38_t1": Workload("38-layer Xing4 MoE trunk, batch 1", 3584, 64, 4, 1024, 1, "bf16", 0.02, n_layers=38),
