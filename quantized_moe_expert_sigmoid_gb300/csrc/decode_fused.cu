@@ -100,12 +100,16 @@ __device__ __forceinline__ float load_x(const void *x, int bf16, int64_t i) {
   return reinterpret_cast<const float *>(x)[i];
 }
 
-// NP > 0: rows of Hp = NP * 512 weights (NP 16-weight positions per lane);
-// NPD > 0: W_down rows of Fp = NPD * 16 weights.  With both known at compile
+// NP > 0: rows of Hp = NP * 512 weights (NP 16-weight positions per lane),
+// at most 64 experts; NPD > 0: W_down rows of Fp = NPD * 16 weights.  With both known at compile
 // time every shared-memory offset in the inner loops is a per-lane base plus
 // an immediate.  NP = NPD = 0: any shape, runtime loops.
 template <int TT, int NP, int NPD>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params p) {
+  // router logits held per lane in the top-k: E <= 64 for the compile-time
+  // Xing4 shape, up to 256 otherwise.  Code that runs once per call comes
+  // from a cold instruction cache, so its length is its cost.
+  constexpr int kNloc = NP > 0 ? 2 : 8;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], wr_bar;
   __shared__ Item items[kMaxItems];
@@ -236,9 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         if (do_route) {
           // selection key: the logit (any bias already added), or in
           // selection mode the sigmoid score plus the bias
-          float v[8];
+          float v[kNloc];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
+          for (int i = 0; i < kNloc; ++i) {
             const int e = lane + 32 * i;
             float l = e < E ? __ldcg(&L.logits[(int64_t)t * E + e]) : -FLT_MAX;
             if (L.sel_bias && e < E) {
@@ -250,9 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           // k rounds of a warp arg-max on order-preserving integer keys:
           // one redux for the largest key, one for the lowest expert id
           // holding it (equal logits go to the lower id)
-          uint32_t key[8];
+          uint32_t key[kNloc];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) key[i] = lane + 32 * i < E ? float_order_key(v[i]) : 0u;
+          for (int i = 0; i < kNloc; ++i) key[i] = lane + 32 * i < E ? float_order_key(v[i]) : 0u;
           unsigned taken = 0;
           uint32_t my_key = 0;
           int my_id = 0;
@@ -261,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
             uint32_t lk = 0;
             int li = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < kNloc; ++i)
               if (i < nloc && !((taken >> i) & 1u) && key[i] > lk) {
                 lk = key[i];
                 li = i;
@@ -546,7 +550,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           const int lofs = (lane >> 4) * kSBBytes + 16 + ((lane >> 1) & 7) * 16 + (lane & 1) * 8;
           const int dofs = (lane >> 4) * kSBBytes + ((lane >> 1) & 7) * 2;
           const int b0 = lane >> 1;
-#pragma unroll
+          // fully unrolled for one or two tokens (more independent work per
+          // warp); rolled for more, where a 7-fold body would leave the
+          // instruction cache
+#pragma unroll (TT <= 2 ? NP : 1)
           for (int k = 0; k < NP; ++k) {
             const uint2 qg = *reinterpret_cast<const uint2 *>(rowg + lofs + 2 * kSBBytes * k);
             const uint2 qu = *reinterpret_cast<const uint2 *>(rowu + lofs + 2 * kSBBytes * k);
@@ -916,7 +923,7 @@ cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, in
   cudaError_t e;
   // compile-time shape for the Xing4 layer (H 3584, F 1024); any other shape
   // takes the runtime-loop instance
-  const bool xing4 = L.Hp == 3584 && L.Fp == 1024;
+  const bool xing4 = L.Hp == 3584 && L.Fp == 1024 && L.E <= 64;
   if (T <= 1)
     e = xing4 ? launch_tt<1, 7, 64>(p, fp.smem, stream) : launch_tt<1, 0, 0>(p, fp.smem, stream);
   else if (T <= 2)
