@@ -92,7 +92,8 @@ struct Layer {
   // opt-in stage timing: kStageEvents events per call slot (see the header)
   cudaEvent_t *tev = nullptr;
   int tev_slots = 0, tev_next = 0, tev_used = 0;
-  CUtensorMap map_x16, map_h16;        // activation tiles of the tensor-core path
+  CUtensorMap map_x16, map_h16;        // activation tiles of the tensor-core path (256 rows)
+  CUtensorMap map_x16_64, map_h16_64;  // ... boxes of 64 rows, for batches of <= 64 tokens
   CUtensorMap map_gu_lab, map_dn_lab;  // weight labels of one k-step
 };
 
@@ -166,6 +167,7 @@ cudaError_t launch_router_tc(const Layer &L, const void *x, int T, const float *
 
 // prefill_tc.cu: grouped GEMMs on tcgen05 for T > kFusedMaxTokens.
 int tc_max_tiles(const Layer &L, bool up_gate);
+int tc_tile_routes(int T);  // routes per tile: 64 for batches of <= 64 tokens, else 256
 cudaError_t tc_prepare(Layer &L);  // tensor maps + kernel attributes (after workspace allocation)
 // ev: nullable; the events to record before up/gate, after up/gate and after down
 cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int T, cudaStream_t stream,

@@ -19,8 +19,9 @@
 // warp-minor order, pass 2 writes each route at base + rank.  Each lane
 // loads 16 routes per round at once, so a pass costs one load round trip
 // per 16,384 routes.  The same CTA then writes the tile lists of the
-// tensor-core path (route tiles of <= 256 per expert, every weight tile of
-// each), from the offsets it holds in shared memory.
+// tensor-core path (route tiles of <= 256 per expert -- <= 64 for batches of
+// up to 64 tokens -- and every weight tile of each), from the offsets it
+// holds in shared memory.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -42,14 +43,13 @@ __device__ __forceinline__ unsigned same_expert_lanes(int e, bool ok) {
   }
   return ok ? peers : 0u;
 }  // routes a lane holds per round (one load round trip)
-constexpr int kTileRoutes = 256;
 
 __global__ void __launch_bounds__(1024) route_plan_kernel(
     const int32_t *__restrict__ ids, const float *__restrict__ wts, int T, int k, int E, int S,
     int *__restrict__ offsets, int *__restrict__ active, int *__restrict__ route_token,
     float *__restrict__ route_weight, unsigned *__restrict__ err, TcTile *__restrict__ ug,
     TcTile *__restrict__ dn, int *__restrict__ tile_counts, int ug_mtiles, int dn_mtiles, int max_ug,
-    int max_dn, int *__restrict__ route_pos) {
+    int max_dn, int *__restrict__ route_pos, int tile_routes) {
   __shared__ int cnt[32 * kMaxE];  // [warp][expert] counts, then bases
   __shared__ int off[kMaxE + 2];
   __shared__ int act[kMaxE + 2];
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(
       else if (e == E && S) c = T;  // the shared expert's segment
       const bool in = e < E + S;
       // inclusive scans of the counts and of the route-tile counts
-      const int ntile = (c + kTileRoutes - 1) / kTileRoutes;
+      const int ntile = (c + tile_routes - 1) / tile_routes;
       int cs = c, ts = ntile;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -184,16 +184,16 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(
     for (int i = tid; i < n_act; i += blockDim.x) {
       const int e = act[i];
       const int beg = off[e], cntr = off[e + 1] - beg;
-      const int nrt = (cntr + kTileRoutes - 1) / kTileRoutes;
+      const int nrt = (cntr + tile_routes - 1) / tile_routes;
       for (int j = 0; j < nrt; ++j) {
-        const int c = min(kTileRoutes, cntr - j * kTileRoutes);
+        const int c = min(tile_routes, cntr - j * tile_routes);
         for (int m = 0; m < ug_mtiles; ++m) {
           const int idx = (tile_base[i] + j) * ug_mtiles + m;
-          if (idx < max_ug) ug[idx] = TcTile{e, m, beg + j * kTileRoutes, c};
+          if (idx < max_ug) ug[idx] = TcTile{e, m, beg + j * tile_routes, c};
         }
         for (int m = 0; m < dn_mtiles; ++m) {
           const int idx = (tile_base[i] + j) * dn_mtiles + m;
-          if (idx < max_dn) dn[idx] = TcTile{e, m, beg + j * kTileRoutes, c};
+          if (idx < max_dn) dn[idx] = TcTile{e, m, beg + j * tile_routes, c};
         }
       }
     }
@@ -212,7 +212,8 @@ cudaError_t launch_route_plan(const Layer &L, const int32_t *ids, const float *w
                                             L.route_token, L.route_weight, L.err, L.tiles_ug,
                                             L.tiles_dn, L.tile_counts, L.Fp / 128, L.Hp / 256,
                                             tc_max_tiles(L, true), tc_max_tiles(L, false),
-                                            L.deterministic ? L.route_pos : nullptr);
+                                            L.deterministic ? L.route_pos : nullptr,
+                                            tc_tile_routes(T));
   count_launches(1);
   return cudaGetLastError();
 }

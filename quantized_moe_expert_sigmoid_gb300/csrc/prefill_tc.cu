@@ -56,10 +56,12 @@ constexpr int kDqWarp0 = 3;         // warps 0..2: activation producer, MMA, wei
 constexpr int kThreadsTC = kDq + 32 * kDqWarp0;
 constexpr int kAStages = 3;
 constexpr int kBStages = 3;
-constexpr int kLabStages = 4;
+constexpr int kLabStages = 4;       // label stages, tiles of up to 256 routes
+constexpr int kLabStagesSmall = 12; // tiles of up to 64 routes: the activation
+                                    // stages shrink to 8 KB and the weight
+                                    // labels get the room (more bytes in flight)
 constexpr int kATile = kTM * kKS * 2;        // 16 KB
 constexpr int kAStage = 2 * kATile;          // 32 KB
-constexpr int kBTile = kNT * kKS * 2;        // 32 KB
 constexpr int kLabStage = kRowsTile * 32;    // labels of one k-step: 32 bytes per row
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait before the CTA gives up
 static_assert(kDq == 2 * kRowsTile, "two dequantising threads per weight row");
@@ -123,15 +125,29 @@ __device__ __forceinline__ int tile_row(int m, int r) {
   return kRowsTile * m + r;
 }
 
+// Shared memory of a configuration: A stages, activation stages of NT rows,
+// label stages.
+template <int NT>
+__host__ __device__ constexpr int tc_lab_stages() { return NT == kNT ? kLabStages : kLabStagesSmall; }
+template <int NT>
+__host__ __device__ constexpr size_t tc_smem_of() {
+  return 1024 + (size_t)kAStages * kAStage + (size_t)kBStages * NT * kKS * 2 +
+         (size_t)tc_lab_stages<NT>() * kLabStage;
+}
+
 // UG = true: up/gate + SwiGLU epilogue; UG = false: down + weighted scatter.
-template <bool UG>
+// NT: routes per tile at most (256; or 64, for batches whose experts all have
+// at most 64 routes).
+template <bool UG, int NT>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     grouped_gemm_tc(const TcParams p, const __grid_constant__ CUtensorMap b_map,
                     const __grid_constant__ CUtensorMap lab_map) {
-  constexpr int kTmemCols = 2 * kNT;
+  constexpr int kTmemCols = 2 * NT;
+  constexpr int kBTileT = NT * kKS * 2;
+  constexpr int kLabSt = tc_lab_stages<NT>();
   extern __shared__ uint8_t smem_dyn[];
   __shared__ uint64_t a_full[kAStages], a_empty[kAStages], b_full[kBStages], b_empty[kBStages],
-      lab_full[kLabStages], lab_empty[kLabStages], acc_full, acc_empty, fin_bar;
+      lab_full[kLabSt], lab_empty[kLabSt], acc_full, acc_empty, fin_bar;
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
   volatile int *abort = &abort_flag;
@@ -144,7 +160,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   // 1 KB of slack for this)
   uint8_t *a_base = smem_dyn + ((1024u - (smem_addr(smem_dyn) & 1023u)) & 1023u);
   uint8_t *b_base = a_base + kAStages * kAStage;
-  uint8_t *lab_base = b_base + kBStages * kBTile;
+  uint8_t *lab_base = b_base + kBStages * kBTileT;
 
   if (tid == 0) {
     for (int s = 0; s < kAStages; ++s) {
@@ -155,7 +171,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
     }
-    for (int s = 0; s < kLabStages; ++s) {
+    for (int s = 0; s < kLabSt; ++s) {
       mbar_init(&lab_full[s], 1);
       mbar_init(&lab_empty[s], kDqWarps);
     }
@@ -181,7 +197,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     // ===================== producers (activations / labels) =====================
     if (lane == 0) {
       const bool act = warp == 0;
-      const int nst = act ? kBStages : kLabStages;
+      const int nst = act ? kBStages : kLabSt;
       uint64_t *full = act ? b_full : lab_full;
       uint64_t *empty = act ? b_empty : lab_empty;
       uint32_t q = 0;
@@ -193,8 +209,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           if (q >= (uint32_t)nst) wait_or_abort(&empty[s], ((q / nst) - 1) & 1u, abort);
           if (*abort) break;
           if (act) {
-            mbar_arrive_expect_tx(&full[s], kBTile);
-            tma_load_2d(b_base + s * kBTile, &b_map, ks * kKS, t.row0, &full[s]);
+            mbar_arrive_expect_tx(&full[s], kBTileT);
+            tma_load_2d(b_base + s * kBTileT, &b_map, ks * kKS, t.row0, &full[s]);
           } else {
             uint8_t *dst = lab_base + s * kLabStage;
             const int xo = (ks >> 2) * kSBBytes + 16 + 32 * (ks & 3);  // blocks 2kk, 2kk+1
@@ -224,7 +240,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       uint32_t q = 0, tcount = 0;
       for (int ti = blockIdx.x; ti < ntiles; ti += gridDim.x, ++tcount) {
         const int count = p.tiles[ti].count;
-        const int n_mma = min(kNT, (count + 15) & ~15);
+        const int n_mma = min(NT, (count + 15) & ~15);
         const uint32_t idesc =
             (1u << 4) | ((uint32_t)(n_mma >> 3) << 17) | ((uint32_t)(kTM >> 4) << 24);
         if (tcount > 0) wait_or_abort(&acc_empty, (tcount - 1) & 1u, abort);  // TMEM drained
@@ -236,12 +252,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           if (*abort) continue;
           tc_fence_after();
           const uint32_t as = smem_addr(a_base + sa * kAStage);
-          const uint32_t bs = smem_addr(b_base + sb * kBTile);
+          const uint32_t bs = smem_addr(b_base + sb * kBTileT);
 #pragma unroll
           for (int a = 0; a < 2; ++a)
 #pragma unroll
             for (int k16 = 0; k16 < kKS / 16; ++k16)
-              umma_f16(tmem + a * kNT, sw128_desc(as + a * kATile + 32 * k16),
+              umma_f16(tmem + a * NT, sw128_desc(as + a * kATile + 32 * k16),
                        sw128_desc(bs + 32 * k16), idesc, (ks | k16) != 0);
           umma_commit(&a_empty[sa]);  // the A stage may be rewritten once these finish
           umma_commit(&b_empty[sb]);  // ... and the B stage refilled
@@ -279,8 +295,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           sc_nxt = __ldg(reinterpret_cast<const uint4 *>(nrowp));
 #pragma unroll
         for (int kk = 0; kk < kKSteps; ++kk, ++q) {
-          const int sl = q % kLabStages;
-          wait_or_abort(&lab_full[sl], (q / kLabStages) & 1u, abort);
+          const int sl = q % kLabSt;
+          wait_or_abort(&lab_full[sl], (q / kLabSt) & 1u, abort);
           const uint4 lab = *reinterpret_cast<const uint4 *>(lab_base + sl * kLabStage + r * 32 + blk * 16);
           __syncwarp();
           if (lane == 0) mbar_arrive(&lab_empty[sl]);  // the labels are in registers
@@ -314,7 +330,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       // A stage -- every MMA of the tile has finished, and no dequantiser
       // writes an A stage again before the barrier closing this epilogue.
       int *ep_tok = reinterpret_cast<int *>(a_base);
-      float *ep_w = reinterpret_cast<float *>(a_base + kNT * sizeof(int));
+      float *ep_w = reinterpret_cast<float *>(a_base + NT * sizeof(int));
       if (!UG) {
         for (int j = dt; j < t.count; j += kDq) {
           ep_tok[j] = p.route_token[t.row0 + j];
@@ -326,10 +342,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const int trow = 32 * quad + lane;  // accumulator row (TMEM lane) of this thread
       const uint32_t tbase = tmem + ((uint32_t)(32 * quad) << 16);
       if (live) {
-        for (int c0 = qc * (kNT / 4); c0 < (qc + 1) * (kNT / 4) && c0 < t.count; c0 += 16) {
+        for (int c0 = qc * (NT / 4); c0 < (qc + 1) * (NT / 4) && c0 < t.count; c0 += 16) {
           uint32_t g[16], u[16];
           tmem_ld16_nowait(tbase + c0, g);
-          tmem_ld16_nowait(tbase + kNT + c0, u);
+          tmem_ld16_nowait(tbase + NT + c0, u);
           tmem_wait_ld();
           if (UG) {
             const int f = t.mtile * kTM + trow;
@@ -464,13 +480,14 @@ cudaError_t encode_2d(CUtensorMap *map, CUtensorMapDataType dt, void *base, uint
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-static size_t tc_smem() {
-  return 1024 + (size_t)kAStages * kAStage + (size_t)kBStages * kBTile + (size_t)kLabStages * kLabStage;
-}
+static_assert(tc_smem_of<kNT>() <= 232448 && tc_smem_of<64>() <= 232448, "shared memory");
 
+
+int tc_tile_routes(int T) { return T <= 64 ? 64 : kNT; }
 
 int tc_max_tiles(const Layer &L, bool up_gate) {
-  const int64_t route_tiles = (int64_t)L.max_routes / kNT + L.E + L.S;
+  // route tiles of 64 (small batches) or 256 routes, plus one partial tile per expert
+  const int64_t route_tiles = (int64_t)L.max_routes / 64 + L.E + L.S;
   return (int)(route_tiles * (up_gate ? L.Fp / kTM : L.Hp / kRowsTile));
 }
 
@@ -490,14 +507,26 @@ cudaError_t tc_prepare(Layer &L) {
     e = encode_2d(&L.map_x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, L.x16, (uint64_t)L.Hp,
                 (uint64_t)L.max_routes, (uint64_t)L.Hp * 2, kKS, kNT, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e == cudaSuccess)
+    e = encode_2d(&L.map_x16_64, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, L.x16, (uint64_t)L.Hp,
+                  (uint64_t)L.max_routes, (uint64_t)L.Hp * 2, kKS, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e == cudaSuccess)
+    e = encode_2d(&L.map_h16_64, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, L.h16, (uint64_t)L.Fp,
+                  (uint64_t)L.max_routes, (uint64_t)L.Fp * 2, kKS, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e == cudaSuccess)
     e = encode_2d(&L.map_h16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, L.h16, (uint64_t)L.Fp,
                   (uint64_t)L.max_routes, (uint64_t)L.Fp * 2, kKS, kNT, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(grouped_gemm_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tc_smem());
+  e = cudaFuncSetAttribute(grouped_gemm_tc<true, kNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tc_smem_of<kNT>());
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(grouped_gemm_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tc_smem());
+    e = cudaFuncSetAttribute(grouped_gemm_tc<false, kNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tc_smem_of<kNT>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_tc<true, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tc_smem_of<64>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_tc<false, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tc_smem_of<64>());
   if (e == cudaSuccess && g_sms_tc == 0) {
     int dev = 0;
     e = cudaGetDevice(&dev);
@@ -539,7 +568,13 @@ cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int 
   p.row_bytes = L.gu_row_bytes;
   p.rows_per_expert = 2 * (int64_t)L.Fp;
   if (ev && (e = cudaEventRecordWithFlags(ev[0], stream, cudaEventRecordExternal)) != cudaSuccess) return e;
-  grouped_gemm_tc<true><<<g_sms_tc, kThreadsTC, tc_smem(), stream>>>(p, L.map_x16, L.map_gu_lab);
+  // batches of at most 64 tokens: route tiles of <= 64 (the plan splits
+  // there), the small-tile configuration
+  const bool small = tc_tile_routes(T) == 64;
+  if (small)
+    grouped_gemm_tc<true, 64><<<g_sms_tc, kThreadsTC, tc_smem_of<64>(), stream>>>(p, L.map_x16_64, L.map_gu_lab);
+  else
+    grouped_gemm_tc<true, kNT><<<g_sms_tc, kThreadsTC, tc_smem_of<kNT>(), stream>>>(p, L.map_x16, L.map_gu_lab);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = cudaEventRecordWithFlags(ev[1], stream, cudaEventRecordExternal)) != cudaSuccess) return e;
@@ -549,7 +584,10 @@ cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int 
   p.w = L.dn;
   p.row_bytes = L.dn_row_bytes;
   p.rows_per_expert = L.Hp;
-  grouped_gemm_tc<false><<<g_sms_tc, kThreadsTC, tc_smem(), stream>>>(p, L.map_h16, L.map_dn_lab);
+  if (small)
+    grouped_gemm_tc<false, 64><<<g_sms_tc, kThreadsTC, tc_smem_of<64>(), stream>>>(p, L.map_h16_64, L.map_dn_lab);
+  else
+    grouped_gemm_tc<false, kNT><<<g_sms_tc, kThreadsTC, tc_smem_of<kNT>(), stream>>>(p, L.map_h16, L.map_dn_lab);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev) return cudaEventRecordWithFlags(ev[2], stream, cudaEventRecordExternal);
