@@ -63,7 +63,7 @@ METRIC = "MoE-layer tokens/s (expert-weight HBM GB/s as fraction of GB300 peak)"
 # changes after its capture).
 NCU_TRAFFIC = {
     "decode1": 32_014_336,        # decode_fused_kernel: profiles/decode_fused_kernel_decode1.md
-    "prefill4096": 456_457_984,   # grouped_gemm_tc<up/gate>: profiles/grouped_gemm_tc_prefill4096.md
+    "prefill4096": 456_259_840,   # grouped_gemm_tc<up/gate>: profiles/grouped_gemm_tc_prefill4096.md
 }
 
 
