@@ -198,8 +198,16 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
     const int e = lane + 32 * i;
     float l = -FLT_MAX, key = -FLT_MAX;
     if (e < E) {
-      l = logits[(int64_t)t * E + e];
-      for (int z = 1; z < parts; ++z) l += logits[(int64_t)z * T * E + (int64_t)t * E + e];
+      // the K-split parts, added in part order; unrolled so that their
+      // loads are in flight together
+      float pz[kRouterMaxParts];
+#pragma unroll
+      for (int z = 0; z < kRouterMaxParts; ++z)
+        pz[z] = z < parts ? logits[(int64_t)z * T * E + (int64_t)t * E + e] : 0.f;
+      l = pz[0];
+#pragma unroll
+      for (int z = 1; z < kRouterMaxParts; ++z)
+        if (z < parts) l += pz[z];
       const float b = bias ? bias[(int64_t)t * bstride + e] : 0.f;
       if (sel) {
         key = 1.0f / (1.0f + expf(-l)) + b;
