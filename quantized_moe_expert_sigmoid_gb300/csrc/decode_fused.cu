@@ -101,7 +101,7 @@ __device__ __forceinline__ float load_x(const void *x, int bf16, int64_t i) {
 }
 
 // NP > 0: rows of Hp = NP * 512 weights (NP 16-weight positions per lane),
-// at most 64 experts; NPD > 0: W_down rows of Fp = NPD * 16 weights.  With both known at compile
+// at most 64 experts, bf16 x; NPD > 0: W_down rows of Fp = NPD * 16 weights.  With both known at compile
 // time every shared-memory offset in the inner loops is a per-lane base plus
 // an immediate.  NP = NPD = 0: any shape, runtime loops.
 template <int TT, int NP, int NPD>
@@ -414,7 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     // =========================== consumer warps ===========================
     const int ct = tid;  // 0 .. kConsumers-1
     pdl_wait();  // x, workspace, outputs and the sync words may come from the previous grid
-    const bool x_staged = p.x_bf16 != 0;
+    // the compile-time Xing4 instance takes bf16 x only (no fp32 code to fetch)
+    const bool x_staged = NP > 0 || p.x_bf16 != 0;
     if (x_staged) {  // one round of 16-byte loads into the xq region (row stride Hp)
       const int h8 = H / 8, hp8 = Hp / 8;
       for (int j0 = ct; j0 < T * hp8; j0 += 4 * kConsumers) {
@@ -620,16 +621,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
       }
     };
 
-    int i = 0;
+    // The up/gate items through one call site: the shared expert's, known
+    // from the start, then the routed ones once the producer has planned
+    // them -- one copy of the item code, which the shared items have
+    // already brought into the instruction cache when the routed ones run.
+    int i = 0, n_ug = n_shared_items;
+    bool planned = false;
     const int my_group = warp / kGroupWarps;  // up/gate items rotate among the warp groups
-    for (; i < n_shared_items; ++i)
+#pragma unroll 1
+    for (;; ++i) {
+      if (i == n_shared_items && !planned) {
+        // the producer warp plans meanwhile; a hardware barrier (it arrives
+        // on every path) leaves it all the issue slots
+        named_sync(kBarPlan, kThreads);
+        planned = true;
+        n_ug = (status & 1) ? i : n_items;
+        while (n_ug > i && items[n_ug - 1].kind != 0) --n_ug;
+      }
+      if (i >= n_ug) break;
       if (i % kItemGroups == my_group) process_upgate(i);
-    // the producer warp plans meanwhile; a hardware barrier (it arrives on
-    // every path) leaves it all the issue slots
-    named_sync(kBarPlan, kThreads);
+    }
     if (!(status & 1)) {
-      for (; i < n_items && items[i].kind == 0; ++i)
-        if (i % kItemGroups == my_group) process_upgate(i);
 
       // ---- every CTA's h written ----
       named_sync(kBarConsumers, kConsumers);
@@ -923,7 +935,7 @@ cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, in
   cudaError_t e;
   // compile-time shape for the Xing4 layer (H 3584, F 1024); any other shape
   // takes the runtime-loop instance
-  const bool xing4 = L.Hp == 3584 && L.Fp == 1024 && L.E <= 64;
+  const bool xing4 = L.Hp == 3584 && L.Fp == 1024 && L.E <= 64 && xdt == MOE_DT_BF16;
   if (T <= 1)
     e = xing4 ? launch_tt<1, 7, 64>(p, fp.smem, stream) : launch_tt<1, 0, 0>(p, fp.smem, stream);
   else if (T <= 2)
