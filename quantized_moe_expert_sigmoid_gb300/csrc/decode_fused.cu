@@ -400,10 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     named_arrive(kBarPlan, kThreads);  // the tables above are visible to the consumers
     if (lane == 0) {
       int i = issued;
-      for (; i < n_items && i < nst; ++i) issue(i);  // stages never used yet
       for (; i < n_items; ++i) {
-        const int s = i % nst;
-        if (!mbar_wait_suspend(&empty_bar[s], (uint32_t)((i / nst) - 1) & 1u, kWaitNs)) {
+        const int s = i % nst;  // a stage's first use needs no wait
+        if (i >= nst && !mbar_wait_suspend(&empty_bar[s], (uint32_t)((i / nst) - 1) & 1u, kWaitNs)) {
           atomicOr(&status, 2);
           break;
         }
