@@ -463,19 +463,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           if (lane == 0) red[warp][t] = v;
         }
         named_sync(kBarConsumers, kConsumers);
-        if (warp == 0) {  // the 16 warp partials of each token, one more warp sum
-          for (int t = 0; t < T; ++t) {
-            float v = warp_sum(lane < kConsumerWarps ? red[lane][t] : 0.f);
-            if (lane == 0) {
-              if (p.bias && !L.sel_bias) v += p.bias[(int64_t)t * p.bstride + e];
-              L.logits[(int64_t)t * E + e] = v;
-            }
-          }
+        if (warp == 0 && lane < T) {  // token `lane`: the warp partials added in warp order
+          float v = red[0][lane];
+          for (int w = 1; w < kConsumerWarps; ++w) v += red[w][lane];
+          if (p.bias && !L.sel_bias) v += p.bias[(int64_t)lane * p.bstride + e];
+          L.logits[(int64_t)lane * E + e] = v;
         }
         named_sync(kBarConsumers, kConsumers);  // `red` is reused by the next expert
       }
-      // this CTA's logits were all written by thread 0: a release add
-      // publishes them (the producers read them after an acquire)
+      // this CTA's logits were written by warp 0 before the barrier above: a
+      // release add publishes them (the producers read them after an acquire)
       if (ct == 0) red_release_add(&p.sync[0], 1u);
     }
     named_sync(kBarConsumers, kConsumers);  // router done with the raw x
