@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           uint32_t my_key = 0;
           int my_id = 0;
           const int nloc = (E + 31) >> 5;  // logits per lane
+#pragma unroll 1  // unrolled, this once-per-call loop costs more instruction fetch than it saves
           for (int j = 0; j < K; ++j) {
             uint32_t lk = 0;
             int li = 0;
