@@ -58,7 +58,6 @@ constexpr int kMaxSlots = kFusedMaxTokens * 9;  // T shared + T*k routed (k <= 8
 constexpr int kMaxEx = kFusedMaxTokens * 8 + 2;
 constexpr int kMaxRowsCta = 32;
 constexpr int kUnits = 3;  // down-phase (row, 16-weight) units per consumer thread
-constexpr int kH4 = 4;     // float4 loads in flight per thread when gathering h
 constexpr uint32_t kPollLimit = 1u << 24;
 constexpr uint32_t kSpinLimit = 1u << 21;
 constexpr int kBarConsumers = 1;  // named barrier ids (0 is __syncthreads)
@@ -104,6 +103,28 @@ __device__ __forceinline__ float load_x(const void *x, int bf16, int64_t i) {
 // at most 64 experts, bf16 x; NPD > 0: W_down rows of Fp = NPD * 16 weights.  With both known at compile
 // time every shared-memory offset in the inner loops is a per-lane base plus
 // an immediate.  NP = NPD = 0: any shape, runtime loops.
+// One item's weight rows into a ring stage: gate rows in the stage's first
+// half and up rows in its second (kind 0), or W_down rows (kind 1).  A call,
+// not inlined: the producer issues from three places, and one copy of the
+// code, warm after the first item, is shorter than three cold ones.
+__device__ __noinline__ void issue_copy(const Item it, int eid, uint8_t *dst, uint64_t *bar,
+                                        const uint8_t *gu, const uint8_t *dn, int64_t gu_eb, int64_t dn_eb,
+                                        int64_t rb, int64_t db, int fpi) {
+  if (it.kind == 0) {
+    const uint8_t *base = gu + (int64_t)eid * gu_eb;
+    const int64_t grow = (int64_t)(it.f0 / kGroupRows) * (2 * kGroupRows) + it.f0 % kGroupRows;
+    const uint32_t bytes = (uint32_t)(it.count * rb);
+    mbar_arrive_expect_tx(bar, 2 * bytes);
+    bulk_g2s(dst, base + grow * rb, bytes, bar);
+    bulk_g2s(dst + fpi * rb, base + (grow + kGroupRows) * rb, bytes, bar);
+  } else {
+    const uint8_t *base = dn + (int64_t)eid * dn_eb + (int64_t)it.f0 * db;
+    const uint32_t bytes = (uint32_t)(it.count * db);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(dst, base, bytes, bar);
+  }
+}
+
 template <int TT, int NP, int NPD>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params p) {
   // router logits held per lane in the top-k: E <= 64 for the compile-time
@@ -180,21 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     auto issue = [&](int i) {
       const Item it = items[i];
       const int s = i % nst;
-      uint8_t *dst = ring + (size_t)s * kStage;
-      const int eid = ex_id[it.a];
-      if (it.kind == 0) {
-        const uint8_t *base = L.gu + (int64_t)eid * L.gu_expert_bytes;
-        const int64_t grow = (int64_t)(it.f0 / kGroupRows) * (2 * kGroupRows) + it.f0 % kGroupRows;
-        const uint32_t bytes = (uint32_t)(it.count * rb);
-        mbar_arrive_expect_tx(&full_bar[s], 2 * bytes);
-        bulk_g2s(dst, base + grow * rb, bytes, &full_bar[s]);
-        bulk_g2s(dst + p.fpi * rb, base + (grow + kGroupRows) * rb, bytes, &full_bar[s]);
-      } else {
-        const uint8_t *base = L.dn + (int64_t)eid * L.dn_expert_bytes + (int64_t)it.f0 * db;
-        const uint32_t bytes = (uint32_t)(it.count * db);
-        mbar_arrive_expect_tx(&full_bar[s], bytes);
-        bulk_g2s(dst, base, bytes, &full_bar[s]);
-      }
+      issue_copy(it, ex_id[it.a], ring + (size_t)s * kStage, &full_bar[s], L.gu, L.dn, L.gu_expert_bytes,
+                 L.dn_expert_bytes, rb, db, p.fpi);
     };
     int issued = 0;
     if (lane == 0) {
@@ -673,6 +681,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           const int f4 = Fp / 4;
           const int total4 = (ex_rs[ge] - rs) * f4;
           const float4 *src = reinterpret_cast<const float4 *>(L.h32 + (int64_t)rs * Fp);
+          // float4 loads in flight per thread: at one token, 2 cover the
+          // five 1,024-wide h rows of the Xing4 layer in one pass
+          constexpr int kH4 = TT == 1 ? 2 : 4;
           for (int base = 0; base < total4; base += kConsumers * kH4) {
             float4 v[kH4];
 #pragma unroll
@@ -779,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
       // every consumer is past its last stage, and are added in group order.
       named_sync(kBarConsumers, kConsumers);
       float *part = reinterpret_cast<float *>(ring);  // [units / g][TT]
-      const int g = (npd & 31) == 0 ? 32 : 16;
+      const int g = ((NPD > 0 ? NPD : npd) & 31) == 0 ? 32 : 16;
 #pragma unroll
       for (int m = 0; m < kUnits; ++m) {
         const int u = ct + kConsumers * m;
