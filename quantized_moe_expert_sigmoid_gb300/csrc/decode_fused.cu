@@ -486,46 +486,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     }
     named_sync(kBarConsumers, kConsumers);  // router done with the raw x
 
-    // ---- quantise x: one thread per 32-element block, in place ----
-    for (int idx = ct; idx < T * hb; idx += kConsumers) {
-      const int t = idx / hb, b = idx % hb;
-      float v[32];
+    // ---- quantise x in place: four threads per 32-element block, eight
+    // elements each, the block maximum taken over the four by shuffles ----
+    const int nq = T * hb * 4;
+    for (int base = 0; base < nq; base += kConsumers) {
+      const int j = base + ct, blk = j >> 2, t = blk / hb, b = blk % hb, e0 = b * 32 + (j & 3) * 8;
+      float v[8];
       if (x_staged) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(xq + (size_t)t * Hp + b * 32);
+        const uint4 w =
+            j < nq ? *reinterpret_cast<const uint4 *>(xq + (size_t)t * Hp + e0) : make_uint4(0, 0, 0, 0);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 w = src[k];
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            v[8 * k + 2 * m] = __uint_as_float(ww[m] << 16);
-            v[8 * k + 2 * m + 1] = __uint_as_float(ww[m] & 0xFFFF0000u);
-          }
+        for (int m = 0; m < 4; ++m) {
+          v[2 * m] = __uint_as_float(ww[m] << 16);
+          v[2 * m + 1] = __uint_as_float(ww[m] & 0xFFFF0000u);
         }
       } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int col = b * 32 + k;
-          v[k] = col < H ? load_x(p.x, 0, (int64_t)t * H + col) : 0.f;
-        }
+        for (int k = 0; k < 8; ++k)
+          v[k] = j < nq && e0 + k < H ? load_x(p.x, 0, (int64_t)t * H + e0 + k) : 0.f;
       }
       float m = 0.f;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) m = fmaxf(m, fabsf(v[k]));
-      const float sc = act_block_scale(m);
-      const float inv = __uint_as_float((uint32_t)(254u << 23) - __float_as_uint(sc));
-      uint32_t packed[16];
+      for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(v[k]));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      if (j < nq) {
+        const float sc = act_block_scale(m);
+        const float inv = __uint_as_float((uint32_t)(254u << 23) - __float_as_uint(sc));
+        uint32_t packed[4];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int q0 = max(-32767, min(32767, __float2int_rn(v[2 * k] * inv)));
-        const int q1 = max(-32767, min(32767, __float2int_rn(v[2 * k + 1] * inv)));
-        packed[k] = (uint32_t)(q0 & 0xFFFF) | ((uint32_t)q1 << 16);
+        for (int k = 0; k < 4; ++k) {
+          const int q0 = max(-32767, min(32767, __float2int_rn(v[2 * k] * inv)));
+          const int q1 = max(-32767, min(32767, __float2int_rn(v[2 * k + 1] * inv)));
+          packed[k] = (uint32_t)(q0 & 0xFFFF) | ((uint32_t)q1 << 16);
+        }
+        *reinterpret_cast<uint4 *>(xq + (size_t)t * Hp + e0) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        if ((j & 3) == 0) sx[(size_t)t * hb + b] = sc;
       }
-      uint4 *dst = reinterpret_cast<uint4 *>(xq + (size_t)t * Hp + b * 32);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        dst[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
-      sx[(size_t)t * hb + b] = sc;
     }
     named_sync(kBarConsumers, kConsumers);
 
