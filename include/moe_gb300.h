@@ -249,6 +249,21 @@ int64_t moe_launch_count(void);
 moe_status moe_layer_enable_timing(moe_layer_t layer, int32_t calls);
 moe_status moe_layer_stage_times(moe_layer_t layer, float *ms, int32_t max_calls, int32_t *n);
 
+/* Test hook for the device-wait error path (no counterpart in the pages).
+ *
+ * moe_test_barrier_slack(layer, 1) makes the single-launch decode kernel
+ * (batches of up to 8 tokens) expect one arrival more than its grid has at
+ * its second grid-wide wait (every CTA's h written), so that the wait can
+ * never be met: every CTA polls up to its bounded limit (2^21 reads of the
+ * counter, well under a minute), then finishes the call without the missing
+ * arrival; moe_layer_check() returns MOE_ERR_TIMEOUT and the call's output
+ * must not be used.  The layer stays usable: slack 0 restores normal calls.
+ * Applies to calls enqueued after it returns (a captured graph keeps the
+ * value it was captured with); the tensor-core path has no grid-wide wait
+ * and ignores it.  MOE_ERR_INVALID_ARG for a NULL layer or a slack other
+ * than 0 or 1. */
+moe_status moe_test_barrier_slack(moe_layer_t layer, int32_t slack);
+
 /* Static name of a status code. */
 const char *moe_status_string(moe_status status);
 

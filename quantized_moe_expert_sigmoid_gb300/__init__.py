@@ -88,10 +88,12 @@ def load_library(path: str | None = None):
     lib.moe_last_error.argtypes = []
     lib.moe_last_error.restype = ctypes.c_char_p
     lib.moe_layer_enable_timing.argtypes = [P, I32]
+    lib.moe_test_barrier_slack.argtypes = [P, I32]
     lib.moe_layer_stage_times.argtypes = [P, P, I32, ctypes.POINTER(I32)]
     for n in ("moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
               "moe_layer_forward_routed", "moe_residual_rmsnorm", "moe_layer_check",
-              "moe_layer_enable_timing", "moe_layer_stage_times", "moe_dense_forward"):
+              "moe_layer_enable_timing", "moe_layer_stage_times", "moe_dense_forward",
+              "moe_test_barrier_slack"):
         getattr(lib, n).restype = I32
     _lib = lib
     return lib
@@ -249,6 +251,13 @@ def moe_layer_enable_timing(layer, calls: int):
     """Record per-stage CUDA events for the next calls on the layer (a ring of
     `calls` slots; 0 disables)."""
     _check(load_library().moe_layer_enable_timing(ctypes.c_void_p(layer), int(calls)))
+
+
+def moe_test_barrier_slack(layer, slack: int):
+    """Test hook: slack 1 makes the single-launch decode kernel's h wait run
+    out (the call then reports MOE_ERR_TIMEOUT through moe_layer_check);
+    0 restores normal calls."""
+    _check(load_library().moe_test_barrier_slack(ctypes.c_void_p(layer), int(slack)))
 
 
 STAGES = ("route+plan+gather", "up/gate", "down", "combine")

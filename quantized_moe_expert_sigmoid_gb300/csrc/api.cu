@@ -441,6 +441,14 @@ moe_status moe_layer_stage_times(moe_layer_t layer, float *ms, int32_t max_calls
   return MOE_OK;
 }
 
+moe_status moe_test_barrier_slack(moe_layer_t layer, int32_t slack) {
+  Layer *L = reinterpret_cast<Layer *>(layer);
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+  if (slack < 0 || slack > 1) return fail(MOE_ERR_INVALID_ARG, "slack = %d: need 0 or 1", slack);
+  L->barrier_slack = slack;
+  return MOE_OK;
+}
+
 moe_status moe_layer_check(moe_layer_t layer) {
   Layer *L = reinterpret_cast<Layer *>(layer);
   if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], wr_bar;
   __shared__ Item items[kMaxItems];
-  __shared__ int n_items, n_shared_items, n_ex, status;
+  __shared__ int n_items, n_shared_items, n_ex, status, n_issued;
   __shared__ int r_tok[kMaxSlots];
   __shared__ float r_w[kMaxSlots];
   __shared__ int ex_id[kMaxEx], ex_rs[kMaxEx + 1];
@@ -417,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         }
         issue(i);
       }
+      n_issued = i;
     }
   } else {
     // =========================== consumer warps ===========================
@@ -651,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
       named_sync(kBarConsumers, kConsumers);
       if (ct == 0) {
         red_release_add(&p.sync[1], 1u);  // every consumer's h, ordered by the barrier above
-        if (!spin_until_geq(&p.sync[1], (unsigned)G, kSpinLimit)) {
+        if (!spin_until_geq(&p.sync[1], (unsigned)(G + L.barrier_slack), kSpinLimit)) {
           atomicOr(&status, 1);
           atomicOr(L.err, kErrTimeout);
         }
@@ -822,6 +823,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
   }
 
   __syncthreads();
+  if (tid == kProducerWarp * 32 && (status & 3)) {
+    // a wait gave up, so consumers may have skipped items: the copies issued
+    // into the ring (the last nst, one per stage) land before the CTA exits
+    for (int j = max(0, n_issued - nst); j < n_issued; ++j)
+      if (!mbar_wait_suspend(&full_bar[j % nst], (uint32_t)(j / nst) & 1u, kWaitNs)) break;
+  }
   if (tid == 0) {
     if (status & 2) atomicOr(L.err, kErrTimeout);
     __threadfence();

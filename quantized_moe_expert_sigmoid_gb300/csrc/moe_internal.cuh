@@ -83,6 +83,7 @@ struct Layer {
   float *dense_w = nullptr;      // [max_tokens] ones
   unsigned *err = nullptr;   // sticky device error word
   unsigned *sync = nullptr;  // [4] arrival counters of the single-launch decode kernel
+  int barrier_slack = 0;     // extra arrivals the decode kernel's h wait expects (test hook)
 
   // batched tensor-core path (T > kFusedMaxTokens)
   __half *x16 = nullptr;     // [max_routes][Hp] x rows in route order, fp16

@@ -88,6 +88,7 @@ def test_known_flags_are_accepted(lib, flags):
 
 def test_null_layer_rejected(lib):
     assert lib.moe_layer_check(None) == 1
+    assert lib.moe_test_barrier_slack(None, 0) == 1
     assert lib.moe_route(None, None, 0, 0, None, None, 0, None, None, None) == 1
     assert lib.moe_forward(None, None, 0, 0, None, None, None, 0, None) == 1
     assert lib.moe_layer_destroy(None) == 0
