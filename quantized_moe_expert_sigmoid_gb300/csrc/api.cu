@@ -74,7 +74,7 @@ void free_layer(Layer *L) {
   void *ptrs[] = {L->gu, L->dn, L->logits, L->offsets, L->active, L->route_token,
                   L->route_weight, L->h32, L->out_acc, L->err, L->sync, L->x16, L->h16,
                   L->tiles_ug, L->tiles_dn, L->tile_counts, L->ybuf, L->route_pos,
-                  L->dense_ids, L->dense_w};
+                  L->dense_ids, L->dense_w, L->rlog};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   if (L->tev) {
@@ -253,6 +253,7 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   ALLOC(L->out_acc, sizeof(float) * (int64_t)sh->max_tokens * H);
   ALLOC(L->err, sizeof(unsigned));
   ALLOC(L->sync, 4 * sizeof(unsigned));
+  ALLOC(L->rlog, sizeof(unsigned long long) * moe::kLogitCopies * moe::kFusedMaxTokens * E);
   // batched tensor-core path (also taken by small batches whose shape the
   // single-launch decode kernel does not cover)
   ALLOC(L->x16, sizeof(__half) * (int64_t)L->max_routes * L->Hp);
@@ -279,6 +280,9 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
     if (e == cudaSuccess) e = moe::launch_fill(L->dense_w, 1.0f, sh->max_tokens, st);
   }
   if (e == cudaSuccess) e = cudaMemsetAsync(L->sync, 0, 4 * sizeof(unsigned), st);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(L->rlog, 0,
+                        sizeof(unsigned long long) * moe::kLogitCopies * moe::kFusedMaxTokens * E, st);
   const int64_t up_bytes = (int64_t)F * (H / 32) * 18;
   const int64_t dn_bytes = (int64_t)H * (F / 32) * 18;
   for (int x = 0; x < E + S && e == cudaSuccess; ++x) {

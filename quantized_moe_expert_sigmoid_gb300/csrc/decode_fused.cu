@@ -63,6 +63,7 @@ constexpr uint32_t kSpinLimit = 1u << 21;
 constexpr int kBarConsumers = 1;  // named barrier ids (0 is __syncthreads)
 constexpr int kBarPlan = 2;       // producer -> consumers: route plan written
 constexpr uint64_t kWaitNs = 500000000ull;  // 0.5 s per copy wait before giving up
+constexpr uint32_t kLogitTag = 1u;  // high word of a router logit written in this call
 
 struct Params {
   Layer L;
@@ -79,7 +80,7 @@ struct Params {
   int nstage, fpi;
   int wr_rows_smem;  // router rows held in the last ring stage (0: read from global)
   int hq_cap;        // routes whose quantised h fit in shared memory at once
-  unsigned *sync;    // [0] router arrivals, [1] h arrivals, [2] exits
+  unsigned *sync;    // [1] h arrivals, [2] exits ([0] unused)
 };
 
 struct Item {
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], wr_bar;
   __shared__ Item items[kMaxItems];
-  __shared__ int n_items, n_shared_items, n_ex, status, n_issued;
+  __shared__ int n_items, n_shared_items, n_ex, status, n_issued, last_cta;
   __shared__ int r_tok[kMaxSlots];
   __shared__ float r_w[kMaxSlots];
   __shared__ int ex_id[kMaxEx], ex_rs[kMaxEx + 1];
@@ -234,25 +235,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     pdl_wait();
 
     bool ok = true;
-    if (do_route) {
-      if (lane == 0) ok = spin_until_geq(&p.sync[0], (unsigned)min(E, G), kSpinLimit);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok && lane == 0) {
-        atomicOr(&status, 1);
-        atomicOr(L.err, kErrTimeout);
-      }
-    }
-    if (ok) {
+    {
       // ---- top-k of every token (every CTA computes the same selection) ----
-      for (int t = 0; t < T; ++t) {
+      for (int t = 0; t < T && ok; ++t) {
         if (do_route) {
+          // The router CTAs store each logit with a tag in the word's high
+          // half (one single-copy-atomic 64-bit store, no fence), into
+          // kLogitCopies copies so that each copy's lines are polled by a
+          // few CTAs only: poll this CTA's copy until every one of the
+          // token's E words carries the tag, with a pause between rounds
+          // (bounded).
+          float lraw[kNloc];
+          bool have = false;
+          for (uint32_t poll = 0; poll < kSpinLimit && !have; ++poll) {
+            bool mine = true;
+#pragma unroll
+            for (int i = 0; i < kNloc; ++i) {
+              const int e = lane + 32 * i;
+              lraw[i] = -FLT_MAX;
+              if (e < E) {
+                const unsigned long long w =
+                    ld_relaxed_u64(&L.rlog[((c % kLogitCopies) * kFusedMaxTokens + t) * E + e]);
+                mine &= (uint32_t)(w >> 32) == kLogitTag;
+                lraw[i] = __uint_as_float((uint32_t)w);
+              }
+            }
+            have = __all_sync(0xffffffffu, mine);
+            if (!have) __nanosleep(384);
+          }
+          if (!have) {
+            ok = false;
+            break;
+          }
           // selection key: the logit (any bias already added), or in
           // selection mode the sigmoid score plus the bias
           float v[kNloc];
 #pragma unroll
           for (int i = 0; i < kNloc; ++i) {
             const int e = lane + 32 * i;
-            float l = e < E ? __ldcg(&L.logits[(int64_t)t * E + e]) : -FLT_MAX;
+            float l = lraw[i];
             if (L.sel_bias && e < E) {
               l = 1.0f / (1.0f + expf(-l));
               if (p.bias) l += p.bias[(int64_t)t * p.bstride + e];
@@ -291,9 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           // the k scores in parallel, lane j holding the j-th (selection
           // mode: from the winner's unbiased logit)
           float my_l = float_from_order_key(my_key);
-          if (L.sel_bias && lane < K) {
-            my_l = __ldcg(&L.logits[(int64_t)t * E + my_id]);
-            if (my_l != my_l) my_l = -FLT_MAX;
+          if (L.sel_bias) {
+            float wl = -FLT_MAX;  // the winner's logit, from the lane that holds it
+#pragma unroll
+            for (int i = 0; i < kNloc; ++i) {
+              const float li = __shfl_sync(0xffffffffu, lraw[i], my_id & 31);
+              if (i == (my_id >> 5)) wl = li;
+            }
+            if (lane < K) my_l = (wl == wl) ? wl : -FLT_MAX;
           }
           const float my_s = lane < K ? 1.0f / (1.0f + expf(-my_l)) : 0.f;
           const float ssum = warp_sum(my_s);
@@ -314,6 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           sel_w[t][lane] = p.w_in[(int64_t)t * K + lane];
         }
       }
+      if (!ok && lane == 0) {
+        atomicOr(&status, 1);
+        atomicOr(L.err, kErrTimeout);
+      }
+    }
+    if (ok) {
       __syncwarp();
       // ---- route plan: routes sorted by (expert, token), by rank ----
       const int R = T * K;
@@ -477,13 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           float v = red[0][lane];
           for (int w = 1; w < kConsumerWarps; ++w) v += red[w][lane];
           if (p.bias && !L.sel_bias) v += p.bias[(int64_t)lane * p.bstride + e];
-          L.logits[(int64_t)lane * E + e] = v;
+          // value and tag in one word: the readers need no other ordering
+          for (int r = 0; r < kLogitCopies; ++r)
+            st_relaxed_u64(&L.rlog[(r * kFusedMaxTokens + lane) * E + e],
+                           ((unsigned long long)kLogitTag << 32) | __float_as_uint(v));
         }
         named_sync(kBarConsumers, kConsumers);  // `red` is reused by the next expert
       }
-      // this CTA's logits were written by warp 0 before the barrier above: a
-      // release add publishes them (the producers read them after an acquire)
-      if (ct == 0) red_release_add(&p.sync[0], 1u);
     }
     named_sync(kBarConsumers, kConsumers);  // router done with the raw x
 
@@ -832,13 +864,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
   if (tid == 0) {
     if (status & 2) atomicOr(L.err, kErrTimeout);
     __threadfence();
-    const unsigned v = atomicAdd(&p.sync[2], 1u);
-    if (v == (unsigned)G - 1) {  // last CTA out resets the words for the next call
-      p.sync[0] = 0;
+    last_cta = atomicAdd(&p.sync[2], 1u) == (unsigned)G - 1;
+  }
+  __syncthreads();
+  if (last_cta) {  // last CTA out resets the words for the next call
+    for (int j = tid; j < kLogitCopies * T * E; j += kThreads)
+      L.rlog[(j / (T * E)) * kFusedMaxTokens * E + j % (T * E)] = 0ull;
+    if (tid == 0) {
       p.sync[1] = 0;
       p.sync[2] = 0;
-      __threadfence();
     }
+    __threadfence();
   }
 }
 

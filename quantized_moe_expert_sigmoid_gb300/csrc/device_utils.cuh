@@ -171,6 +171,18 @@ __device__ __forceinline__ uint32_t ld_acquire(const unsigned *p) {
   return v;
 }
 
+// Relaxed 64-bit global load / store at GPU scope: single-copy atomic for an
+// aligned word, and never served from a stale L1 line.
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // Spin until *ctr >= target (acquire), at most `limit` polls.  Each poll is
 // an L2 round trip (several hundred ns), which bounds the wait in time; no
 // sleep between polls, which measured faster for the batched decode call.

@@ -34,6 +34,7 @@ constexpr int kGroupRows = 64;  // gate/up interleave group
 
 // Largest batch the single-launch decode kernel handles.
 constexpr int kFusedMaxTokens = 8;
+constexpr int kLogitCopies = 8;  // copies of the decode kernel's tagged router logits
 
 // Sticky device error bits (Layer::err).
 constexpr unsigned kErrBadId = 1u;
@@ -83,6 +84,7 @@ struct Layer {
   float *dense_w = nullptr;      // [max_tokens] ones
   unsigned *err = nullptr;   // sticky device error word
   unsigned *sync = nullptr;  // [4] arrival counters of the single-launch decode kernel
+  unsigned long long *rlog = nullptr;  // [kLogitCopies][kFusedMaxTokens][E] tagged router logits
   int barrier_slack = 0;     // extra arrivals the decode kernel's h wait expects (test hook)
 
   // batched tensor-core path (T > kFusedMaxTokens)
