@@ -15,17 +15,18 @@
 //             32 KB shared-memory stages (full/empty mbarriers per stage);
 //             before the programmatic-dependent-launch wait it already
 //             fetches this CTA's slice of the shared expert's up/gate rows
-//             and its router row (weights are immutable); then it waits
-//             (bounded) for every router logit, selects the top-k of every
-//             token, builds the route plan and issues the routed experts'
-//             up/gate rows and this CTA's rows of every W_down.
+//             and its router row (weights are immutable); then it polls
+//             (bounded) until every router logit has been written (each a
+//             tagged 64-bit word), selects the top-k of every token, builds
+//             the route plan and issues the routed experts' up/gate rows and
+//             this CTA's rows of every W_down.
 //   consumers stage x, compute the router logit of expert `blockIdx.x`,
 //             quantise x to 16-bit integers per 32-block (power-of-two
 //             scale), stream the up/gate items (three groups of 8 warps
 //             take alternate items; warp w computes the gate and the up row
 //             of output f0 + w % 8, applies SwiGLU and writes h to global
-//             memory), wait
-//             (bounded) until every CTA has written its h, then own output
+//             memory), wait (bounded) until every CTA has written its h
+//             (a grid-wide counter), then own output
 //             rows [c*H/G, (c+1)*H/G): every consumer thread keeps fixed
 //             (row, 16-weight) units of W_down, accumulates them over all
 //             experts (route weight folded into the activation scale) and the
@@ -100,10 +101,6 @@ __device__ __forceinline__ float load_x(const void *x, int bf16, int64_t i) {
   return reinterpret_cast<const float *>(x)[i];
 }
 
-// NP > 0: rows of Hp = NP * 512 weights (NP 16-weight positions per lane),
-// at most 64 experts, bf16 x; NPD > 0: W_down rows of Fp = NPD * 16 weights.  With both known at compile
-// time every shared-memory offset in the inner loops is a per-lane base plus
-// an immediate.  NP = NPD = 0: any shape, runtime loops.
 // One item's weight rows into a ring stage: gate rows in the stage's first
 // half and up rows in its second (kind 0), or W_down rows (kind 1).  A call,
 // not inlined: the producer issues from three places, and one copy of the
@@ -126,6 +123,11 @@ __device__ __noinline__ void issue_copy(const Item it, int eid, uint8_t *dst, ui
   }
 }
 
+// NP > 0: rows of Hp = NP * 512 weights (NP 16-weight positions per lane),
+// at most 64 experts, bf16 x; NPD > 0: W_down rows of Fp = NPD * 16 weights.
+// With both known at compile time every shared-memory offset in the inner
+// loops is a per-lane base plus an immediate.  NP = NPD = 0: any shape,
+// runtime loops.
 template <int TT, int NP, int NPD>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params p) {
   // router logits held per lane in the top-k: E <= 64 for the compile-time
