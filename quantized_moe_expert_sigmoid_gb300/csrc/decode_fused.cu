@@ -152,13 +152,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
   const int G = gridDim.x, c = blockIdx.x;
   const int Hp = L.Hp, Fp = L.Fp, H = L.H, E = L.E, S = L.S, K = L.k;
   const int64_t rb = L.gu_row_bytes, db = L.dn_row_bytes;
-  const int nst = p.nstage, hb = Hp / 32, fb32 = Fp / 32;
+  // divisors known at compile time in the Xing4 instance
+  const int nst = p.nstage, hb = NP > 0 ? NP * 16 : Hp / 32, fb32 = Fp / 32;
   uint8_t *ring = smem;
   int16_t *xq = reinterpret_cast<int16_t *>(smem + (size_t)nst * kStage);
   float *sx = reinterpret_cast<float *>(xq + (size_t)T * Hp);
   int16_t *hq = reinterpret_cast<int16_t *>(sx + (size_t)T * hb);
   float *shs = reinterpret_cast<float *>(hq + (size_t)p.hq_cap * Fp);
-  const int n0 = (int)((int64_t)c * H / G), n1 = (int)((int64_t)(c + 1) * H / G);
+  // 32-bit splits (H * G, Fp * G and the routed rows * G stay below 2^32;
+  // a 64-bit division is a long software sequence)
+  const unsigned uG = (unsigned)G;
+  const int n0 = (int)((unsigned)c * (unsigned)H / uG), n1 = (int)((unsigned)(c + 1) * (unsigned)H / uG);
   const int nrows = n1 - n0;
   const bool do_route = p.ids_in == nullptr;
 
@@ -193,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         r_w[t] = 1.0f;
         rid[0][t] = (int8_t)t;
       }
-      add_upgate(0, (int)((int64_t)c * Fp / G), (int)((int64_t)(c + 1) * Fp / G));
+      add_upgate(0, (int)((unsigned)c * (unsigned)Fp / uG), (int)((unsigned)(c + 1) * (unsigned)Fp / uG));
     }
     n_shared_items = n_items;
   }
@@ -414,12 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
         // at once, before the rest of the plan.
         int ni = n_items;
         const int D = nex - S;
-        const int64_t N = (int64_t)D * Fp;
-        const int64_t fb = (int64_t)c * N / G, fe = (int64_t)(c + 1) * N / G;
+        const unsigned N = (unsigned)D * (unsigned)Fp;
+        const int fb = (int)((unsigned)c * N / uG), fe = (int)((unsigned)(c + 1) * N / uG);
         for (int a = S; a < nex; ++a) {
-          const int64_t lo = (int64_t)(a - S) * Fp, hi = lo + Fp;
-          int f = (int)(max(fb, lo) - lo);
-          const int f_end = (int)(min(fe, hi) - lo);
+          const int lo = (a - S) * Fp, hi = lo + Fp;
+          int f = max(fb, lo) - lo;
+          const int f_end = min(fe, hi) - lo;
           while (f < f_end && ni < kMaxItems) {
             const int grp_end = (f / kGroupRows + 1) * kGroupRows;
             const int cnt = min(min(f_end, grp_end) - f, p.fpi);
@@ -460,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     // the compile-time Xing4 instance takes bf16 x only (no fp32 code to fetch)
     const bool x_staged = NP > 0 || p.x_bf16 != 0;
     if (x_staged) {  // one round of 16-byte loads into the xq region (row stride Hp)
-      const int h8 = H / 8, hp8 = Hp / 8;
+      const int h8 = H / 8, hp8 = NP > 0 ? NP * 64 : Hp / 8;
       for (int j0 = ct; j0 < T * hp8; j0 += 4 * kConsumers) {
         uint4 v[4];
 #pragma unroll
@@ -712,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           if (grp_end >= 0) named_sync(kBarConsumers, kConsumers);  // previous group no longer read
           int ge = a + 1;
           while (ge < n_ex && ex_rs[ge + 1] - rs <= p.hq_cap) ++ge;
-          const int f4 = Fp / 4;
+          const int f4 = NPD > 0 ? NPD * 4 : Fp / 4;
           const int total4 = (ex_rs[ge] - rs) * f4;
           const float4 *src = reinterpret_cast<const float4 *>(L.h32 + (int64_t)rs * Fp);
           // float4 loads in flight per thread: at one token, 2 cover the
@@ -896,6 +900,9 @@ bool plan_fused(const Layer &L, int T, FusedPlan &fp) {
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
   }
+  // the kernel splits rows among the CTAs in 32-bit arithmetic
+  const int64_t d_max = std::min<int64_t>((int64_t)T * L.k, L.E);
+  if ((int64_t)std::max<int64_t>(L.H, d_max * L.Fp) * g_sms >= (int64_t)1 << 32) return false;
   fp.fpi = (int)std::min<int64_t>(8, kStage / (2 * L.gu_row_bytes));
   if (fp.fpi < 1) return false;
   const int rows_cta = (L.H + g_sms - 1) / g_sms;
