@@ -66,6 +66,10 @@ constexpr int kBarPlan = 2;       // producer -> consumers: route plan written
 constexpr uint64_t kWaitNs = 500000000ull;  // 0.5 s per copy wait before giving up
 constexpr uint32_t kLogitTag = 1u;  // high word of a router logit written in this call
 
+// Ring depth of the compile-time Xing4 instances (the launcher checks that
+// the shared-memory plan gave this depth): 6 stages up to two tokens, 3 above.
+__host__ __device__ constexpr int xing4_stages(int tt) { return tt <= 2 ? 6 : 3; }
+
 struct Params {
   Layer L;
   const void *x;
@@ -148,12 +152,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
   __shared__ float red[kConsumerWarps][TT];
 
   const Layer &L = p.L;
-  const int T = p.T, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the one-token instance is only launched for T = 1
+  const int T = TT == 1 ? 1 : p.T, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, c = blockIdx.x;
   const int Hp = L.Hp, Fp = L.Fp, H = L.H, E = L.E, S = L.S, K = L.k;
   const int64_t rb = L.gu_row_bytes, db = L.dn_row_bytes;
   // divisors known at compile time in the Xing4 instance
-  const int nst = p.nstage, hb = NP > 0 ? NP * 16 : Hp / 32, fb32 = Fp / 32;
+  const int nst = NP > 0 ? xing4_stages(TT) : p.nstage, hb = NP > 0 ? NP * 16 : Hp / 32, fb32 = Fp / 32;
   uint8_t *ring = smem;
   int16_t *xq = reinterpret_cast<int16_t *>(smem + (size_t)nst * kStage);
   float *sx = reinterpret_cast<float *>(xq + (size_t)T * Hp);
@@ -699,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
       pdl_launch_dependents();
 
       // ---- W_down rows of this CTA, summed over all experts ----
-      const int npd = Fp / 16;  // 16-weight units per row
+      const int npd = NPD > 0 ? NPD : Fp / 16;  // 16-weight units per row
       float acc[kUnits][TT];
 #pragma unroll
       for (int m = 0; m < kUnits; ++m)
@@ -848,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
       named_sync(kBarConsumers, kConsumers);
       const int gpr = npd / g;  // groups per row
       for (int idx = ct; idx < nrows * T; idx += kConsumers) {
-        const int t = idx / nrows, rr = idx % nrows;
+        const int t = TT == 1 ? 0 : idx / nrows, rr = TT == 1 ? idx : idx % nrows;
         float v = part[(rr * gpr) * TT + t];
         for (int j = 1; j < gpr; ++j) v += part[(rr * gpr + j) * TT + t];
         const int64_t o = (int64_t)t * H + n0 + rr;
@@ -994,7 +999,9 @@ cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, in
   cudaError_t e;
   // compile-time shape for the Xing4 layer (H 3584, F 1024); any other shape
   // takes the runtime-loop instance
-  const bool xing4 = L.Hp == 3584 && L.Fp == 1024 && L.E <= 64 && xdt == MOE_DT_BF16;
+  const int tt = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
+  const bool xing4 = L.Hp == 3584 && L.Fp == 1024 && L.E <= 64 && xdt == MOE_DT_BF16 &&
+                     fp.nstage == xing4_stages(tt);
   if (T <= 1)
     e = xing4 ? launch_tt<1, 7, 64>(p, fp.smem, stream) : launch_tt<1, 0, 0>(p, fp.smem, stream);
   else if (T <= 2)
