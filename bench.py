@@ -62,8 +62,11 @@ METRIC = "MoE-layer tokens/s (expert-weight HBM GB/s as fraction of GB300 peak)"
 # from the ncu captures summarised in profiles/ (set to None when the kernel
 # changes after its capture).
 NCU_TRAFFIC = {
-    "decode1": 31_980_544,        # decode_fused_kernel: profiles/decode_fused_kernel_decode1.md
-    "prefill4096": 457_219_328,   # grouped_gemm_tc<up/gate>: profiles/grouped_gemm_tc_prefill4096.md
+    # decode_fused_kernel changed (fewer instructions, the same copies) after
+    # its last ncu capture, which read 31,980,544 B per launch: null until it
+    # is captured again
+    "decode1": None,
+    "prefill4096": 457_219_328,   # grouped_gemm_tc<up/gate>, ncu dram read + write per launch
 }
 
 
