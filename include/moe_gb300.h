@@ -100,6 +100,11 @@ typedef struct {
  * of up to 8 tokens are deterministic with or without the flag. */
 #define MOE_FLAG_DETERMINISTIC 2u
 
+/* Host input and output for moe_layer_forward_routed_host: the layer holds
+ * a device copy buffer for x and one for out, each max_tokens * hidden * 4
+ * bytes, allocated at create. */
+#define MOE_FLAG_HOST_IO 4u
+
 /* Expert weights in IQ4_NL blocks (18 bytes each, no alignment needed).
  *   up, gate: [E][F][H/32] blocks     down: [E][H][F/32] blocks
  *   sh_up, sh_gate: [F][H/32]         sh_down: [H][F/32]  (NULL if no shared)
@@ -180,6 +185,21 @@ moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype 
                                     const float *logit_bias, int64_t bias_row_stride,
                                     int32_t *ids, float *weights, void *out,
                                     moe_dtype out_dtype, void *stream);
+
+/* moe_layer_forward_routed with x and out in host memory, for a layer
+ * created with MOE_FLAG_HOST_IO: one call copies x (T * hidden elements of
+ * x_dtype) into the layer's device buffer, runs the layer, and copies out
+ * back, all enqueued on `stream` (cudaMemcpyAsync; x_host and out_host
+ * should be page-locked for the copies to be asynchronous, and stay valid
+ * and untouched until the stream has passed the call).  router_w,
+ * logit_bias, ids and weights are device pointers as for
+ * moe_layer_forward_routed.  MOE_ERR_INVALID_ARG for a layer without the
+ * flag or a NULL host pointer; otherwise errors as for
+ * moe_layer_forward_routed. */
+moe_status moe_layer_forward_routed_host(moe_layer_t layer, const void *x_host, moe_dtype x_dtype,
+                                         int32_t T, const float *router_w, const float *logit_bias,
+                                         int64_t bias_row_stride, int32_t *ids, float *weights,
+                                         void *out_host, moe_dtype out_dtype, void *stream);
 
 /* Residual update and RMS normalisation between stacked layers (PocketLLM
  * design record, section 2: the residual stream is carried in fp32 and the

@@ -20,6 +20,7 @@ MOE_DT_BF16 = 0
 MOE_DT_FP32 = 1
 MOE_FLAG_SELECTION_BIAS = 1  # the bias ranks experts only (noaux_tc); weights stay unbiased
 MOE_FLAG_DETERMINISTIC = 2   # slot-ordered combine: equal inputs give equal output bits
+MOE_FLAG_HOST_IO = 4         # device copy buffers for moe_layer_forward_routed_host
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_OUT_OF_MEMORY", 5: "MOE_ERR_CUDA",
@@ -75,6 +76,7 @@ def load_library(path: str | None = None):
     lib.moe_forward.argtypes = [P, P, I32, I32, P, P, P, I32, P]
     lib.moe_dense_forward.argtypes = [P, P, I32, I32, P, I32, P]
     lib.moe_layer_forward_routed.argtypes = [P, P, I32, I32, P, P, I64, P, P, P, I32, P]
+    lib.moe_layer_forward_routed_host.argtypes = [P, P, I32, I32, P, P, I64, P, P, P, I32, P]
     lib.moe_residual_rmsnorm.argtypes = [P, P, I32, P, I32, I32, F, P]
     lib.moe_layer_check.argtypes = [P]
     lib.moe_layer_weight_bytes.argtypes = [P]
@@ -93,7 +95,7 @@ def load_library(path: str | None = None):
     for n in ("moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
               "moe_layer_forward_routed", "moe_residual_rmsnorm", "moe_layer_check",
               "moe_layer_enable_timing", "moe_layer_stage_times", "moe_dense_forward",
-              "moe_test_barrier_slack"):
+              "moe_test_barrier_slack", "moe_layer_forward_routed_host"):
         getattr(lib, n).restype = I32
     _lib = lib
     return lib
@@ -208,6 +210,38 @@ def moe_layer_forward_routed(layer, x, router_w, ids, weights, out, logit_bias=N
         _ptr(router_w, "router_w", d["f32"]), bias_p, bias_row_stride,
         _ptr(ids, "ids", d["i32"]), _ptr(weights, "weights", d["f32"]), _ptr(out, "out", d["x"]),
         _dtype(out), _stream(stream)))
+
+
+def _host_ptr(t, name, dtypes):
+    """Host pointer of a dense CPU tensor (page-locked for asynchronous copies)."""
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (row-major); got strides {tuple(t.stride())}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be in host memory")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def moe_layer_forward_routed_host(layer, x_host, router_w, ids, weights, out_host, logit_bias=None,
+                                  bias_row_stride=None, stream=None):
+    """moe_layer_forward_routed with x and out in host memory (pinned CPU
+    tensors), for a layer created with MOE_FLAG_HOST_IO: the copies in and
+    out are enqueued on the stream with the layer call; out_host is written
+    once the stream has passed the call."""
+    if bias_row_stride is None:
+        bias_row_stride = 0 if logit_bias is None or logit_bias.dim() == 1 else logit_bias.stride(0)
+    d = _dt()
+    if logit_bias is not None and logit_bias.dim() == 2 and logit_bias.stride(1) == 1 \
+            and bias_row_stride == logit_bias.stride(0):
+        bias_p = ctypes.c_void_p(logit_bias.data_ptr())
+    else:
+        bias_p = _ptr(logit_bias, "logit_bias", d["f32"])
+    _check(load_library().moe_layer_forward_routed_host(
+        ctypes.c_void_p(layer), _host_ptr(x_host, "x_host", d["x"]), _dtype(x_host), x_host.shape[0],
+        _ptr(router_w, "router_w", d["f32"]), bias_p, bias_row_stride,
+        _ptr(ids, "ids", d["i32"]), _ptr(weights, "weights", d["f32"]),
+        _host_ptr(out_host, "out_host", d["x"]), _dtype(out_host), _stream(stream)))
 
 
 def moe_route_noalloc(x, router_w, ids, weights, top_k, routed_scaling=2.0, logit_bias=None,

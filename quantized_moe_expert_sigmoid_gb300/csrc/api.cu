@@ -74,7 +74,7 @@ void free_layer(Layer *L) {
   void *ptrs[] = {L->gu, L->dn, L->logits, L->offsets, L->active, L->route_token,
                   L->route_weight, L->h32, L->out_acc, L->err, L->sync, L->x16, L->h16,
                   L->tiles_ug, L->tiles_dn, L->tile_counts, L->ybuf, L->route_pos,
-                  L->dense_ids, L->dense_w, L->rlog};
+                  L->dense_ids, L->dense_w, L->rlog, L->x_stage, L->out_stage};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   if (L->tev) {
@@ -208,7 +208,7 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   if (S != 0 && S != 1) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "n_shared = %d: need 0 or 1", S);
   if (!(sh->routed_scaling > 0.f)) return fail(MOE_ERR_INVALID_ARG, "routed_scaling must be > 0");
   if (sh->max_tokens < 1 || sh->max_tokens > 65536) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "max_tokens = %d: need 1..65536", sh->max_tokens);
-  if (sh->flags & ~(MOE_FLAG_SELECTION_BIAS | MOE_FLAG_DETERMINISTIC))
+  if (sh->flags & ~(MOE_FLAG_SELECTION_BIAS | MOE_FLAG_DETERMINISTIC | MOE_FLAG_HOST_IO))
     return fail(MOE_ERR_INVALID_ARG, "flags = 0x%x: unknown bits", sh->flags);
   if (!wt->up || !wt->gate || !wt->down) return fail(MOE_ERR_INVALID_ARG, "up, gate and down must be non-NULL");
   if (S && (!wt->sh_up || !wt->sh_gate || !wt->sh_down)) return fail(MOE_ERR_INVALID_ARG, "shared expert weights must be non-NULL when n_shared = 1");
@@ -254,6 +254,10 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   ALLOC(L->err, sizeof(unsigned));
   ALLOC(L->sync, 4 * sizeof(unsigned));
   ALLOC(L->rlog, sizeof(unsigned long long) * moe::kLogitCopies * moe::kFusedMaxTokens * E);
+  if (sh->flags & MOE_FLAG_HOST_IO) {
+    ALLOC(L->x_stage, sizeof(float) * (int64_t)sh->max_tokens * H);
+    ALLOC(L->out_stage, sizeof(float) * (int64_t)sh->max_tokens * H);
+  }
   // batched tensor-core path (also taken by small batches whose shape the
   // single-launch decode kernel does not cover)
   ALLOC(L->x16, sizeof(__half) * (int64_t)L->max_routes * L->Hp);
@@ -386,6 +390,36 @@ moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype 
   s = forward_impl(L, x, x_dtype, T, ids, weights, out, out_dtype, st, ev, true);
   if (s == MOE_OK && ev) timing_advance(L);
   return s;
+}
+
+moe_status moe_layer_forward_routed_host(moe_layer_t layer, const void *x_host, moe_dtype x_dtype,
+                                         int32_t T, const float *router_w, const float *logit_bias,
+                                         int64_t bias_row_stride, int32_t *ids, float *weights,
+                                         void *out_host, moe_dtype out_dtype, void *stream) {
+  Layer *L = reinterpret_cast<Layer *>(layer);
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+  if (!L->x_stage || !L->out_stage)
+    return fail(MOE_ERR_INVALID_ARG, "the layer was not created with MOE_FLAG_HOST_IO");
+  if (x_dtype != MOE_DT_BF16 && x_dtype != MOE_DT_FP32)
+    return fail(MOE_ERR_INVALID_ARG, "x_dtype %d is not MOE_DT_BF16 or MOE_DT_FP32", (int)x_dtype);
+  if (out_dtype != MOE_DT_BF16 && out_dtype != MOE_DT_FP32)
+    return fail(MOE_ERR_INVALID_ARG, "out_dtype %d is not MOE_DT_BF16 or MOE_DT_FP32", (int)out_dtype);
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d is negative", T);
+  if (T > L->max_tokens)
+    return fail(MOE_ERR_TOO_MANY_TOKENS, "T = %d exceeds max_tokens = %d", T, L->max_tokens);
+  if (T == 0) return MOE_OK;
+  if (!x_host || !out_host) return fail(MOE_ERR_INVALID_ARG, "x_host and out_host must be non-NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t n = (size_t)T * L->H;
+  MOE_CUDA(cudaMemcpyAsync(L->x_stage, x_host, n * (x_dtype == MOE_DT_BF16 ? 2 : 4), cudaMemcpyHostToDevice, st),
+           "copy x to the device");
+  const moe_status s = moe_layer_forward_routed(layer, L->x_stage, x_dtype, T, router_w, logit_bias,
+                                                bias_row_stride, ids, weights, L->out_stage, out_dtype, stream);
+  if (s != MOE_OK) return s;
+  MOE_CUDA(cudaMemcpyAsync(out_host, L->out_stage, n * (out_dtype == MOE_DT_BF16 ? 2 : 4),
+                           cudaMemcpyDeviceToHost, st),
+           "copy out to the host");
+  return MOE_OK;
 }
 
 moe_status moe_residual_rmsnorm(float *resid, const void *delta, moe_dtype delta_dtype, void *u,

@@ -85,6 +85,7 @@ struct Layer {
   unsigned *err = nullptr;   // sticky device error word
   unsigned *sync = nullptr;  // [4] arrival counters of the single-launch decode kernel
   unsigned long long *rlog = nullptr;  // [kLogitCopies][kFusedMaxTokens][E] tagged router logits
+  void *x_stage = nullptr, *out_stage = nullptr;  // [max_tokens][H] x 4 B each (MOE_FLAG_HOST_IO)
   int barrier_slack = 0;     // extra arrivals the decode kernel's h wait expects (test hook)
 
   // batched tensor-core path (T > kFusedMaxTokens)
