@@ -405,9 +405,11 @@ template <typename XT>
 __global__ void gather_x16_kernel(const XT *__restrict__ x, const int *__restrict__ route_token,
                                   const int *__restrict__ total, int H, int Hp, int max_rows,
                                   __half *__restrict__ x16, unsigned *err) {
-  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;  // one 8-element chunk
-  const int hp8 = Hp / 8;
-  const int64_t row = i / hp8;
+  // one 8-element chunk; the launcher keeps max_rows * Hp / 8 below 2^32, so
+  // the row split is a 32-bit division (a 64-bit one is a long sequence)
+  const unsigned i = blockIdx.x * blockDim.x + threadIdx.x;
+  const unsigned hp8 = (unsigned)Hp / 8u;
+  const int row = (int)(i / hp8);
   const int c8 = (int)(i % hp8);
   if (row >= max_rows || row >= *total) return;
   float v[8];
@@ -541,6 +543,7 @@ cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int 
   cudaError_t e;
   // gather x in route order as fp16
   const int64_t chunks = (int64_t)max_rows * (L.Hp / 8);
+  if (chunks + 255 >= ((int64_t)1 << 32)) return cudaErrorInvalidValue;  // 32-bit chunk index
   const int gb = (int)((chunks + 255) / 256);
   if (xdt == MOE_DT_BF16)
     gather_x16_kernel<__nv_bfloat16><<<gb, 256, 0, stream>>>(
