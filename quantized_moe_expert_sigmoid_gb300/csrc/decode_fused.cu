@@ -159,6 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
   const int64_t rb = L.gu_row_bytes, db = L.dn_row_bytes;
   // divisors known at compile time in the Xing4 instance
   const int nst = NP > 0 ? xing4_stages(TT) : p.nstage, hb = NP > 0 ? NP * 16 : Hp / 32, fb32 = Fp / 32;
+  // ring stage and round of item i: the depth is 3 or 6, so both are
+  // divisions by a constant (a runtime divisor costs a long sequence)
+  auto stage_of = [nst](int i) { return nst == 6 ? i % 6 : i % 3; };
+  auto round_of = [nst](int i) { return nst == 6 ? i / 6 : i / 3; };
   uint8_t *ring = smem;
   int16_t *xq = reinterpret_cast<int16_t *>(smem + (size_t)nst * kStage);
   float *sx = reinterpret_cast<float *>(xq + (size_t)T * Hp);
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     // =========================== producer warp ===========================
     auto issue = [&](int i) {
       const Item it = items[i];
-      const int s = i % nst;
+      const int s = stage_of(i);
       issue_copy(it, ex_id[it.a], ring + (size_t)s * kStage, &full_bar[s], L.gu, L.dn, L.gu_expert_bytes,
                  L.dn_expert_bytes, rb, db, p.fpi);
     };
@@ -453,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     if (lane == 0) {
       int i = issued;
       for (; i < n_items; ++i) {
-        const int s = i % nst;  // a stage's first use needs no wait
-        if (i >= nst && !mbar_wait_suspend(&empty_bar[s], (uint32_t)((i / nst) - 1) & 1u, kWaitNs)) {
+        const int s = stage_of(i);  // a stage's first use needs no wait
+        if (i >= nst && !mbar_wait_suspend(&empty_bar[s], (uint32_t)(round_of(i) - 1) & 1u, kWaitNs)) {
           atomicOr(&status, 2);
           break;
         }
@@ -581,8 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     // on the stage's "empty" barrier (its count is all the consumer warps).
     auto process_upgate = [&](int i) {
       const Item it = items[i];
-      const int s = i % nst;
-      if (!mbar_wait_suspend(&full_bar[s], (uint32_t)(i / nst) & 1u, kWaitNs)) atomicOr(&status, 2);
+      const int s = stage_of(i);
+      if (!mbar_wait_suspend(&full_bar[s], (uint32_t)round_of(i) & 1u, kWaitNs)) atomicOr(&status, 2);
       const int rs = ex_rs[it.a], nr = ex_rs[it.a + 1] - rs;
       const int fl = warp % kGroupWarps;
       float accg[TT], accu[TT];
@@ -760,8 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           named_sync(kBarConsumers, kConsumers);
         }
         const int hoff = rs - grp_rs;
-        const int s = i % nst;
-        if (!mbar_wait_suspend(&full_bar[s], (uint32_t)(i / nst) & 1u, kWaitNs)) atomicOr(&status, 2);
+        const int s = stage_of(i);
+        if (!mbar_wait_suspend(&full_bar[s], (uint32_t)round_of(i) & 1u, kWaitNs)) atomicOr(&status, 2);
         int rids[TT];
 #pragma unroll
         for (int t = 0; t < TT; ++t) rids[t] = t < T ? (int)rid[a][t] : -1;
@@ -870,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     // a wait gave up, so consumers may have skipped items: the copies issued
     // into the ring (the last nst, one per stage) land before the CTA exits
     for (int j = max(0, n_issued - nst); j < n_issued; ++j)
-      if (!mbar_wait_suspend(&full_bar[j % nst], (uint32_t)(j / nst) & 1u, kWaitNs)) break;
+      if (!mbar_wait_suspend(&full_bar[stage_of(j)], (uint32_t)round_of(j) & 1u, kWaitNs)) break;
   }
   if (tid == 0) {
     if (status & 2) atomicOr(L.err, kErrTimeout);
@@ -922,7 +926,7 @@ bool plan_fused(const Layer &L, int T, FusedPlan &fp) {
   // exact when the stage's previous use was that group's too
   fp.nstage = (int)std::min<size_t>(kMaxStages, (limit - fixed - (size_t)T * per_route) / kStage);
   fp.nstage -= fp.nstage % kItemGroups;
-  if (fp.nstage < kItemGroups) return false;
+  if (fp.nstage != 3 && fp.nstage != 6) return false;  // the kernel divides by 3 or 6 only
   const size_t left = limit - fixed - (size_t)fp.nstage * kStage;
   fp.hq_cap = (int)std::min<size_t>((size_t)T * (L.k + L.S), left / per_route);
   fp.smem = fixed + (size_t)fp.nstage * kStage + (size_t)fp.hq_cap * per_route;
