@@ -216,14 +216,19 @@ moe_status moe_residual_rmsnorm(float *resid, const void *delta, moe_dtype delta
  * cudaMalloc themselves or let a library do it -- code inside a host
  * framework that owns every device allocation, a stream-ordered pool that
  * must not grow, or a serving step that may not allocate once it is up.
- * It computes exactly what moe_route computes (same kernels, same arguments
- * and layouts, no layer object), but its fp32 logits scratch is a fixed
+ * It computes what moe_route computes (same arguments and layouts, no layer
+ * object) on the CUDA-core router kernels; moe_route takes batches of 256
+ * or more bf16 tokens (n_experts <= 128) to a tensor-core router instead.
+ * Both select from fp32 logits, so their ids agree wherever a token's top
+ * k+1 scores are further apart than the logits' rounding (~1e-6) and their
+ * weights agree to about 1e-6.  Its fp32 logits scratch is a fixed
  * file-scope device array of 262,144 floats (1 MiB) that every GPU which
  * loads the library keeps until the process exits.
  *   T * n_experts > 262,144 returns MOE_ERR_UNSUPPORTED_SHAPE; nothing is
- *   allocated or freed.  The first call on a device looks up the array's
- *   device address (cudaGetSymbolAddress) and caches it, so make that first
- *   call before any stream capture.  Every call shares the one array: calls
+ *   allocated or freed.  The first call on a device (and the first after a
+ *   cudaDeviceReset, which moves the array) looks up the array's device
+ *   address (cudaGetSymbolAddress) and caches it, so make that first call
+ *   before any stream capture.  Every call shares the one array: calls
  *   whose kernels overlap on the GPU (for example on two streams) race on
  *   it.  The scratch is fully written before it is read, so nothing needs
  *   clearing between calls. */

@@ -16,6 +16,8 @@
 
 #include <algorithm>
 
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -326,22 +328,58 @@ static __device__ __align__(256) float g_noalloc_logits[kNoAllocMaxLogits];
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 float *g_noalloc_ptr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};  // context the cached address belongs to
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+
+// Unique id of the calling thread's current context (driver entry points
+// resolved once, under g_noalloc_mu).  A cudaDeviceReset ends the context;
+// the next one gets a new id, and the module -- with the array -- is loaded
+// again at a new address.
+cudaError_t current_context_id(unsigned long long *id) {
+  if (!g_ctx_current || !g_ctx_id) {
+    void *f1 = nullptr, *f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 4000, cudaEnableDefault, &q1);
+    if (e == cudaSuccess)
+      e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
+    if (e != cudaSuccess) return e;
+    if (q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+      return cudaErrorNotSupported;
+    g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f1);
+    g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+  return g_ctx_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is asked of
-// the runtime once per device (with that device current) and cached.
+// the runtime (with that device current) and cached per device, together
+// with the id of the context it was taken in; a call in a later context of
+// the same device (after a cudaDeviceReset) looks the address up again.
 cudaError_t noalloc_scratch(float **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void *ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_logits);
-    if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = static_cast<float *>(ptr);
+  unsigned long long ctx = 0;
+  if (g_noalloc_ptr[dev] && current_context_id(&ctx) == cudaSuccess && g_noalloc_ctx[dev] == ctx) {
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
   }
+  // first call on this device, or in a new context of it: the lookup also
+  // binds the device's primary context to this thread when none is
+  void *ptr = nullptr;
+  e = cudaGetSymbolAddress(&ptr, g_noalloc_logits);
+  if (e != cudaSuccess) return e;
+  e = current_context_id(&ctx);
+  if (e != cudaSuccess) return e;
+  g_noalloc_ptr[dev] = static_cast<float *>(ptr);
+  g_noalloc_ctx[dev] = ctx;
   *out = g_noalloc_ptr[dev];
   return cudaSuccess;
 }

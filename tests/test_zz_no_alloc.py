@@ -70,3 +70,23 @@ def test_noalloc_router_rejects_more_than_its_scratch():
         moe.moe_route_noalloc(x, wr, ids, w, 2)
     assert e.value.name == "MOE_ERR_UNSUPPORTED_SHAPE"
     assert "scratch" in str(e.value)
+
+
+@pytest.mark.parametrize("T", [256, 4096])
+def test_noalloc_router_large_bf16_batches(T):
+    """At 256 and more bf16 tokens moe_route runs the tensor-core router and
+    moe_route_noalloc the CUDA-core one: both must give the oracle's ids on
+    gap-resampled inputs, and weights within the router tolerance of each
+    other.  T = 4,096 with 64 experts fills the scratch exactly."""
+    wl = synth.Workload(f"router-only: H 3584, 64 experts top-4, {T} tokens", 3584, 64, 4, 32, T,
+                        "bf16", 0.02)
+    ew = synth.expert_weights(0, 0, 64, 3584, 32)
+    layer = MoeLayer.from_weights(ew, k=4, scale=2.0, max_tokens=T)
+    c = cases.make_case(wl, ew=ew)
+    for _ in range(2):  # two calls in a row through the shared scratch
+        ids_a, w_a, ids_b, w_b = _both(layer, c)
+        np.testing.assert_array_equal(ids_a, c.ids)
+        np.testing.assert_array_equal(ids_b, c.ids)
+        np.testing.assert_allclose(w_b, w_a, rtol=0, atol=2e-6)
+        np.testing.assert_allclose(w_b, c.w, rtol=0, atol=2e-6)
+    layer.close()
