@@ -233,6 +233,18 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   L->weight_bytes = (int64_t)(E + S) * 3 * F * (H / 32) * 18;
   L->max_routes = sh->max_tokens * k + S * sh->max_tokens;
   cudaStream_t st = (cudaStream_t)stream;
+  {
+    cudaError_t e0 = cudaGetDevice(&L->device);
+    if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&L->sms, cudaDevAttrMultiProcessorCount, L->device);
+    // kernel attributes of this device, and whether the single-launch decode
+    // grid can be resident at once
+    if (e0 == cudaSuccess) e0 = moe::decode_prepare(*L);
+    if (e0 == cudaSuccess) e0 = moe::router_tc_prepare();
+    if (e0 != cudaSuccess) {
+      free_layer(L);
+      return cuda_fail(e0, "moe_layer_create: device set-up");
+    }
+  }
 
 #define ALLOC(ptr, bytes)                                                          \
   do {                                                                             \

@@ -893,8 +893,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
   }
 }
 
-int g_sms = 0;
-
 struct FusedPlan {
   int fpi, nstage, hq_cap, wr_rows_smem;
   size_t smem;
@@ -904,11 +902,10 @@ struct FusedPlan {
 // single-launch kernel.
 bool plan_fused(const Layer &L, int T, FusedPlan &fp) {
   if (T < 1 || T > kFusedMaxTokens || L.k > 8 || L.E > 256) return false;
-  if (g_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    if (cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-  }
+  // the grid-wide handoffs need every CTA of the grid (one per SM) resident
+  // at once; create checked that one CTA of every instance fits an SM
+  if (!L.fused_resident || L.sms < 1) return false;
+  const int g_sms = L.sms;
   // the kernel splits rows among the CTAs in 32-bit arithmetic
   const int64_t d_max = std::min<int64_t>((int64_t)T * L.k, L.E);
   if ((int64_t)std::max<int64_t>(L.H, d_max * L.Fp) * g_sms >= (int64_t)1 << 32) return false;
@@ -943,18 +940,21 @@ bool plan_fused(const Layer &L, int T, FusedPlan &fp) {
   return items <= kMaxItems;
 }
 
+// Raise the instance's shared-memory limit on the current device and report
+// how many of its CTAs an SM holds at the largest plan (the grid needs 1).
 template <int TT, int NP, int NPD>
-cudaError_t launch_tt(const Params &p, size_t smem, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<TT, NP, NPD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_limit_fused());
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+cudaError_t prepare_tt(int *per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<TT, NP, NPD>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_limit_fused());
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, decode_fused_kernel<TT, NP, NPD>, kThreads,
+                                                       smem_limit_fused());
+}
+
+template <int TT, int NP, int NPD>
+cudaError_t launch_tt(const Params &p, int grid, size_t smem, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(g_sms);
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -969,6 +969,21 @@ cudaError_t launch_tt(const Params &p, size_t smem, cudaStream_t stream) {
 }  // namespace
 
 size_t smem_limit_fused() { return 232448 - 8192; }  // dynamic part; static tables take < 8 KB
+
+cudaError_t decode_prepare(Layer &L) {
+  int n[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  cudaError_t e = prepare_tt<1, 7, 64>(&n[0]);
+  if (e == cudaSuccess) e = prepare_tt<1, 0, 0>(&n[1]);
+  if (e == cudaSuccess) e = prepare_tt<2, 7, 64>(&n[2]);
+  if (e == cudaSuccess) e = prepare_tt<2, 0, 0>(&n[3]);
+  if (e == cudaSuccess) e = prepare_tt<4, 7, 64>(&n[4]);
+  if (e == cudaSuccess) e = prepare_tt<4, 0, 0>(&n[5]);
+  if (e == cudaSuccess) e = prepare_tt<8, 7, 64>(&n[6]);
+  if (e == cudaSuccess) e = prepare_tt<8, 0, 0>(&n[7]);
+  if (e != cudaSuccess) return e;
+  L.fused_resident = *std::min_element(n, n + 8) >= 1 ? 1 : 0;
+  return cudaSuccess;
+}
 
 bool fused_decode_supported(const Layer &L, int T) {
   FusedPlan fp;
@@ -1007,13 +1022,13 @@ cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, in
   const bool xing4 = L.Hp == 3584 && L.Fp == 1024 && L.E <= 64 && xdt == MOE_DT_BF16 &&
                      fp.nstage == xing4_stages(tt);
   if (T <= 1)
-    e = xing4 ? launch_tt<1, 7, 64>(p, fp.smem, stream) : launch_tt<1, 0, 0>(p, fp.smem, stream);
+    e = xing4 ? launch_tt<1, 7, 64>(p, L.sms, fp.smem, stream) : launch_tt<1, 0, 0>(p, L.sms, fp.smem, stream);
   else if (T <= 2)
-    e = xing4 ? launch_tt<2, 7, 64>(p, fp.smem, stream) : launch_tt<2, 0, 0>(p, fp.smem, stream);
+    e = xing4 ? launch_tt<2, 7, 64>(p, L.sms, fp.smem, stream) : launch_tt<2, 0, 0>(p, L.sms, fp.smem, stream);
   else if (T <= 4)
-    e = xing4 ? launch_tt<4, 7, 64>(p, fp.smem, stream) : launch_tt<4, 0, 0>(p, fp.smem, stream);
+    e = xing4 ? launch_tt<4, 7, 64>(p, L.sms, fp.smem, stream) : launch_tt<4, 0, 0>(p, L.sms, fp.smem, stream);
   else
-    e = xing4 ? launch_tt<8, 7, 64>(p, fp.smem, stream) : launch_tt<8, 0, 0>(p, fp.smem, stream);
+    e = xing4 ? launch_tt<8, 7, 64>(p, L.sms, fp.smem, stream) : launch_tt<8, 0, 0>(p, L.sms, fp.smem, stream);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -50,6 +50,12 @@ struct TcTile {
 };
 
 struct Layer {
+  // device the layer was created on, and its SM count (read at create; every
+  // kernel attribute and grid size of the layer's launches comes from them)
+  int device = 0, sms = 0;
+  // the single-launch decode kernel's grid (one CTA per SM) can be resident
+  // all at once: checked at create from the occupancy of every instance
+  int fused_resident = 0;
   // shape
   int H, E, k, F, S;  // S = number of shared experts (0 or 1)
   float scale;
@@ -151,6 +157,9 @@ cudaError_t launch_combine_ordered(const Layer &L, int T, void *out, moe_dtype o
 // ids_in == nullptr: route inside (router_w, bias used; ids_out/w_out
 // written); else the given routes are used.
 size_t smem_limit_fused();
+// kernel attributes and the co-residency check of every decode instance, on
+// the current device (create)
+cudaError_t decode_prepare(Layer &L);
 bool fused_decode_supported(const Layer &L, int T);
 cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, int T,
                                 const float *wr, const float *bias, int64_t bstride,
@@ -165,6 +174,7 @@ cudaError_t encode_2d(CUtensorMap *map, CUtensorMapDataType dt, void *base, uint
 // router_tc.cu: router logits of large bf16 batches on tcgen05 (K-partial
 // sums in the same layout as launch_router_logits).  false: not applicable.
 bool router_tc_supported(const Layer &L, moe_dtype xdt, int T);
+cudaError_t router_tc_prepare();  // kernel attribute, on the current device (create)
 int router_tc_parts(const Layer &L, int T);
 cudaError_t launch_router_tc(const Layer &L, const void *x, int T, const float *wr, float *logits,
                              int parts, cudaStream_t stream);

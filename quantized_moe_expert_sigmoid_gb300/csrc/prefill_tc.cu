@@ -445,8 +445,6 @@ __global__ void gather_x16_kernel(const XT *__restrict__ x, const int *__restric
   *reinterpret_cast<uint4 *>(x16 + row * Hp + c8 * 8) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-int g_sms_tc = 0;
-
 }  // namespace
 
 namespace {
@@ -529,11 +527,6 @@ cudaError_t tc_prepare(Layer &L) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(grouped_gemm_tc<false, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)tc_smem_of<64>());
-  if (e == cudaSuccess && g_sms_tc == 0) {
-    int dev = 0;
-    e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_sms_tc, cudaDevAttrMultiProcessorCount, dev);
-  }
   return e;
 }
 
@@ -575,9 +568,9 @@ cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int 
   // there), the small-tile configuration
   const bool small = tc_tile_routes(T) == 64;
   if (small)
-    grouped_gemm_tc<true, 64><<<g_sms_tc, kThreadsTC, tc_smem_of<64>(), stream>>>(p, L.map_x16_64, L.map_gu_lab);
+    grouped_gemm_tc<true, 64><<<L.sms, kThreadsTC, tc_smem_of<64>(), stream>>>(p, L.map_x16_64, L.map_gu_lab);
   else
-    grouped_gemm_tc<true, kNT><<<g_sms_tc, kThreadsTC, tc_smem_of<kNT>(), stream>>>(p, L.map_x16, L.map_gu_lab);
+    grouped_gemm_tc<true, kNT><<<L.sms, kThreadsTC, tc_smem_of<kNT>(), stream>>>(p, L.map_x16, L.map_gu_lab);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = cudaEventRecordWithFlags(ev[1], stream, cudaEventRecordExternal)) != cudaSuccess) return e;
@@ -588,9 +581,9 @@ cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int 
   p.row_bytes = L.dn_row_bytes;
   p.rows_per_expert = L.Hp;
   if (small)
-    grouped_gemm_tc<false, 64><<<g_sms_tc, kThreadsTC, tc_smem_of<64>(), stream>>>(p, L.map_h16_64, L.map_dn_lab);
+    grouped_gemm_tc<false, 64><<<L.sms, kThreadsTC, tc_smem_of<64>(), stream>>>(p, L.map_h16_64, L.map_dn_lab);
   else
-    grouped_gemm_tc<false, kNT><<<g_sms_tc, kThreadsTC, tc_smem_of<kNT>(), stream>>>(p, L.map_h16, L.map_dn_lab);
+    grouped_gemm_tc<false, kNT><<<L.sms, kThreadsTC, tc_smem_of<kNT>(), stream>>>(p, L.map_h16, L.map_dn_lab);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev) return cudaEventRecordWithFlags(ev[2], stream, cudaEventRecordExternal);

@@ -234,13 +234,7 @@ bool router_tc_supported(const Layer &L, moe_dtype xdt, int T) {
 
 // K parts so that tiles x parts fills the SMs once, none of them empty.
 int router_tc_parts(const Layer &L, int T) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 148;
-  }
+  const int sms = std::max(1, L.sms);
   const int tiles = (T + kRtN - 1) / kRtN;
   const int nks = (L.H + kRtKS - 1) / kRtKS;
   const int want = std::max(1, std::min(std::min(kRouterMaxParts, nks), sms / tiles));
@@ -248,17 +242,14 @@ int router_tc_parts(const Layer &L, int T) {
   return (nks + per - 1) / per;
 }
 
+cudaError_t router_tc_prepare() {
+  return cudaFuncSetAttribute(router_logits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rt_smem());
+}
+
 cudaError_t launch_router_tc(const Layer &L, const void *x, int T, const float *wr, float *logits,
                              int parts, cudaStream_t stream) {
   if (!L.err || parts < 1) return cudaErrorInvalidValue;
-  static bool attr = false;
   cudaError_t e;
-  if (!attr) {
-    if ((e = cudaFuncSetAttribute(router_logits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)rt_smem())) != cudaSuccess)
-      return e;
-    attr = true;
-  }
   CUtensorMap x_map;  // the caller's x: [T][H] bf16, K-major
   if ((e = encode_2d(&x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(x), (uint64_t)L.H,
                      (uint64_t)T, (uint64_t)L.H * 2, kRtKS, kRtN, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
