@@ -3,19 +3,28 @@
 A step is one call of the whole layer (router logits, sigmoid top-k and
 weights, per-expert histogram/scan/permutation, gather, dequantising
 up/gate + SwiGLU, down projection, weighted combine with the shared expert)
-over one batch of synthetic tokens.  Default workload: the Xing4-shaped layer
-at decode batch 1 (H 3584, 64 experts top-4 + 1 shared, F 1024, bf16 x).
+over one batch of synthetic tokens.  Headline workload: the Xing4-shaped
+layer at decode batch 1 (H 3584, 64 experts top-4 + 1 shared, F 1024, bf16
+x).  The default run (one GPU) then measures the other configurations of the
+same layer the same way and reports them under "workloads": the tiny layer,
+batched decode of 64 tokens, the 4,096-token Zipf-skewed prefill, and the
+38-layer trunk at 1 and 16 tokens.
 
-L2: one layer's working set (~32 MB) fits the 129 MB L2, so steps rotate over
-NL resident layers with distinct weights (16 by default: 6.5 GB) and 64
-distinct inputs; the data touched in one rotation (16 x 31.9 MB) is about
-4x the L2, so each step's weights come from HBM.
+L2: one layer's working set (~32 MB at batch 1) fits the 129 MB L2, so
+steps rotate over NL resident layers with distinct weights (16 by default:
+6.5 GB) and 64 distinct inputs; the data touched in one rotation (16 x 31.9
+MB) is about 4x the L2, so each step's weights come from HBM.  Batches of 64
+and more tokens touch ~400 MB per call and rotate over 2 layers; the trunk
+holds its 38 layers (15.3 GB).
 
-Steps run as CUDA-graph replays (G steps per graph) so that the GPU, not
-the Python launch loop, sets the pace; the graph holds exactly the launches
-of G layer calls.  `e2e` times the same calls eagerly, one
-moe_layer_forward_routed_host call per step: the input copied from pinned
-host memory, the layer, and the output copied back, enqueued by the library.
+Steps run as CUDA-graph replays (G steps per graph) so that the GPU, not the
+Python launch loop, sets the pace; the graph holds exactly the launches of G
+layer calls, and the timed region replays it until exactly --steps steps
+have run.  The spread of the step time (p10 / median / p90) comes from a
+further >= 10 replays of the same graph, each timed on its own.  `e2e` times
+the same calls eagerly, one moe_layer_forward_routed_host call per step: the
+input copied from pinned host memory, the layer, and the output copied back,
+enqueued by the library.
 
 --impl reference times the CPU oracle (fp64, single thread) on the same
 workload and metric.
@@ -33,6 +42,10 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# configurations measured beside the decode-1 headline in the default run
+EXTRA_WORKLOADS = ("tiny", "decode64", "prefill4096", "trunk38_t1", "trunk38_t16")
+
+
 def expert_bytes_of(wl):
     """IQ4_NL bytes of one expert: up, gate and down, 18 bytes per 32 weights
     (6,193,152 B for the Xing4 layer)."""
@@ -42,38 +55,59 @@ def expert_bytes_of(wl):
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=65536)
-    p.add_argument("--warmup", type=int, default=64)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="decode1",
-                   choices=["decode1", "decode8", "decode64", "prefill4096", "trunk38_t1", "trunk38_t16",
+                   choices=["tiny", "decode1", "decode8", "decode64", "prefill4096", "trunk38_t1", "trunk38_t16",
                             "k2h_decode1", "k2h_decode64", "k2h_prefill1024"])
     p.add_argument("--layers", type=int, default=16, help="resident layers the steps rotate over")
     p.add_argument("--graph-steps", type=int, default=32)
     p.add_argument("--e2e-steps", type=int, default=2000)
-    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extra", action="store_true",
+                   help="measure the headline workload only (no 'workloads' section)")
     return p.parse_args()
 
 
 METRIC = "MoE-layer tokens/s (expert-weight HBM GB/s as fraction of GB300 peak)"
 
 # DRAM bytes (read + write) per launch of each workload's dominant kernel,
-# from the ncu captures summarised in profiles/ (set to None when the kernel
-# changes after its capture).
+# from the ncu captures summarised in profiles/ (None when the kernel changed
+# after its capture).
 NCU_TRAFFIC = {
-    # decode_fused_kernel changed (fewer instructions, the same copies) after
-    # its last ncu capture, which read 31,980,544 B per launch: null until it
-    # is captured again
+    # decode_fused_kernel changed after its last ncu capture (31,980,544 B
+    # per launch then): null until it is captured again
     "decode1": None,
     "prefill4096": 457_219_328,   # grouped_gemm_tc<up/gate>, ncu dram read + write per launch
 }
 
 
-def bench_config(args, wl, world):
+def load_peaks():
+    """Roofline denominators: MEASURED_PEAKS.json, else the fallback figures."""
+    try:
+        pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return {"hbm": float(pk["hbm_gbs"]), "hbm_src": "measured",
+                "bf16": float(pk["bf16_tflops"]), "bf16_src": "measured burst",
+                "bf16_sus": float(pk["bf16_tflops_sustained"]), "bf16_sus_src": "measured sustained"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm": 6800.0, "hbm_src": "fallback", "bf16": 1900.0, "bf16_src": "fallback burst",
+                "bf16_sus": 1700.0, "bf16_sus_src": "fallback sustained"}
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def bench_config(args, wl, world, steps):
+    """(resident layers, distinct inputs, steps per graph, config dict)."""
     T = wl.T
     if wl.n_layers > 1:
-        G = max(1, min(args.graph_steps, args.steps, 8))
+        G = max(1, min(args.graph_steps, steps, 8))
         return wl.n_layers, 16, G, {
             "workload": wl.name, "tokens_per_step": T, "layers": wl.n_layers, "hidden": wl.H,
             "experts": wl.E, "top_k": wl.k, "expert_ffn": wl.F, "shared_experts": 1,
@@ -84,7 +118,7 @@ def bench_config(args, wl, world):
             "graph_steps": G}
     NL = args.layers if T < 64 else max(1, min(args.layers, 2))
     NX = 64 if T < 64 else 2
-    G = max(1, min(args.graph_steps, args.steps))
+    G = max(1, min(args.graph_steps, steps))
     return NL, NX, G, {
         "workload": wl.name, "tokens_per_step": T, "hidden": wl.H, "experts": wl.E,
         "top_k": wl.k, "expert_ffn": wl.F, "shared_experts": 1, "routed_scaling": wl.scale,
@@ -93,24 +127,17 @@ def bench_config(args, wl, world):
         "graph_steps": G}
 
 
-def replay_percentiles(start, marks, per_replay_steps):
-    """p10 / median / p90 of the per-step time over the graph replays of the
-    timed region (each replay holds per_replay_steps steps), in ms."""
-    if not marks:
-        return None
-    ts, prev = [], start
-    for m in marks:
-        ts.append(prev.elapsed_time(m) / per_replay_steps)
-        prev = m
-    ts.sort()
-    pick = lambda q: ts[min(len(ts) - 1, int(q * (len(ts) - 1) + 0.5))]
-    return {"p10": pick(0.1), "median": pick(0.5), "p90": pick(0.9), "replays": len(ts)}
-
-
 def algorithmic_bytes(wl, T, distinct_experts):
     """HBM bytes one call must move at least: the selected experts' and the
     shared expert's IQ4_NL weights, the fp32 router, x in and out (bf16)."""
     return (distinct_experts + 1) * expert_bytes_of(wl) + wl.E * wl.H * 4 + 2 * T * wl.H * 2
+
+
+def layer_flops(wl, T):
+    """Dense-equivalent flops of one call: 6 H F per route (gate, up, down
+    multiply-adds) for the k routed and the shared expert, plus the fp32
+    router's 2 T E H."""
+    return T * (wl.k + 1) * 6.0 * wl.H * wl.F + 2.0 * T * wl.E * wl.H
 
 
 class Clocks:
@@ -171,19 +198,22 @@ def cpu_baseline(wl_name, seconds):
     oracle.build()
     done, t0 = 0, time.perf_counter()
     while True:
-        x = oracle.to_f64(synth.activations(0, "bench", 1, wl.H, np.array([done])), "bf16")
+        x = oracle.to_f64(synth.activations(0, "bench", 1, wl.H, np.array([done]), wl.x_dtype), wl.x_dtype)
         b = None if bias is None else bias[done % wl.T][None, :]
         oracle.moe_layer(x, wr, ew, wl.k, wl.scale, b)
         done += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
+    cores = host_cores()
     if wl.n_layers > 1:  # a token crosses every layer of the trunk (plus an RMSNorm each)
-        return {"value": done / el / wl.n_layers, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        return {"value": done / el / wl.n_layers, "unit": "tokens/s", "cores": 1, "host_cores": cores,
+                "kind": "oracle",
                 "sample": f"{done} single-token calls of one layer of the {wl_name} trunk "
-                          f"({el:.1f} s, fp64, 1 thread), scaled by its {wl.n_layers} layers"}
-    return {"value": done / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} single-token layer calls of the {wl_name} workload ({el:.1f} s, fp64, 1 thread)"}
+                          f"({el:.1f} s, fp64, 1 thread of {cores}), scaled by its {wl.n_layers} layers"}
+    return {"value": done / el, "unit": "tokens/s", "cores": 1, "host_cores": cores, "kind": "oracle",
+            "sample": f"{done} single-token layer calls of the {wl_name} workload "
+                      f"({el:.1f} s, fp64, 1 thread of {cores})"}
 
 
 def run_reference(args, rank, world):
@@ -193,7 +223,7 @@ def run_reference(args, rank, world):
     wl = synth.WORKLOADS[args.workload]
     budget = 90.0
     r = cpu_baseline(args.workload, min(budget, 3.0 + 0.2 * (args.steps + args.warmup)))
-    _, _, _, cfg = bench_config(args, wl, world)
+    _, _, _, cfg = bench_config(args, wl, world, args.steps)
     line = {"impl": "reference", "metric": METRIC, "value": r["value"],
             "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -205,21 +235,82 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank, world, local_rank):
+def timed_graph_steps(torch, moe, stream, step, steps, G, local_rank, world):
+    """Capture G steps in a graph (and the remainder in a second), replay
+    them so that exactly `steps` steps run in the timed region, bracketed by
+    a barrier and device synchronisations; then time >= 10 further replays
+    one by one for the spread.  Returns (ms, launches in the timed region,
+    clocks summary, percentiles)."""
+    reps, rem = divmod(steps, G)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(n):
+                step(j, j)
+        return g
+
+    l0 = moe.moe_launch_count()
+    g_main = capture(G) if reps else None
+    per_graph = moe.moe_launch_count() - l0
+    l0 = moe.moe_launch_count()
+    g_rem = capture(rem) if rem else None
+    per_rem = moe.moe_launch_count() - l0
+    with torch.cuda.stream(stream):
+        for g in (g_main, g_rem):
+            if g:
+                g.replay()
+    stream.synchronize()
+
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local_rank) as clk:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(reps):
+                g_main.replay()
+            if g_rem:
+                g_rem.replay()
+            stop.record(stream)
+        stop.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = start.elapsed_time(stop)
+
+    # spread: replays of the main graph, each timed on its own (outside the
+    # timed region above)
+    g_spread, n_steps = (g_main, G) if g_main else (g_rem, rem)
+    per_replay_ms = ms / max(1, steps) * n_steps
+    n_rep = int(max(10, min(200, 2000.0 / max(per_replay_ms, 1e-3))))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(n_rep):
+            g_spread.replay()
+            ev[i + 1].record(stream)
+    ev[-1].synchronize()
+    ts = sorted(ev[i].elapsed_time(ev[i + 1]) / n_steps for i in range(n_rep))
+    pick = lambda q: ts[min(len(ts) - 1, int(q * (len(ts) - 1) + 0.5))]
+    pct = {"p10": pick(0.1), "median": pick(0.5), "p90": pick(0.9), "replays": n_rep,
+           "steps_per_replay": n_steps, "where": "replays after the timed region, each timed on its own"}
+    del g_main, g_rem, g_spread
+    return ms, reps * per_graph + (per_rem if rem else 0), clk.summary(), pct
+
+
+def measure_layer(args, name, steps, warmup, world, rank, local_rank, dev, cpu_seconds, headline):
+    """One single-layer workload: bench line fields (value, ms, roofline, ...)."""
     import numpy as np
     import torch
     import quantized_moe_expert_sigmoid_gb300 as moe
-    from quantized_moe_expert_sigmoid_gb300 import build as moe_build, synth
+    from quantized_moe_expert_sigmoid_gb300 import synth
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if rank == 0 or not os.path.exists(moe_build.LIB):
-        moe_build.build()
-    if world > 1:
-        torch.distributed.barrier()
-    wl = synth.WORKLOADS[args.workload]
+    wl = synth.WORKLOADS[name]
     T = wl.T
-    NL, NX, G, cfg = bench_config(args, wl, world)
+    NL, NX, G, cfg = bench_config(args, wl, world, steps)
+    pk = load_peaks()
 
     layers, routers = [], []
     for l in range(NL):
@@ -230,10 +321,16 @@ def run_ours(args, rank, world, local_rank):
         del ew
         routers.append(torch.from_numpy(synth.router_weights(7, l, wl.E, wl.H, wl.router_sigma)).to(dev))
     torch.cuda.empty_cache()
-    xs_host = [synth.activations(100 + rank, "bench", T, wl.H, np.full(T, i)) for i in range(NX)]
-    xs = [torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16) for a in xs_host]
+    xs_host = [synth.activations(100 + rank, "bench", T, wl.H, np.full(T, i), wl.x_dtype) for i in range(NX)]
+    xdt = torch.bfloat16 if wl.x_dtype == "bf16" else torch.float32
+
+    def to_x(a, device=None):
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if wl.x_dtype == "bf16" else torch.from_numpy(a)
+        return t.to(device) if device is not None else t
+
+    xs = [to_x(a, dev) for a in xs_host]
     bias = torch.from_numpy(synth.zipf_logit_bias(7, T, wl.E)).to(dev) if wl.zipf else None
-    outs = [torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev) for _ in range(G)]
+    outs = [torch.empty((T, wl.H), dtype=xdt, device=dev) for _ in range(G)]
     ids = [torch.empty((T, wl.k), dtype=torch.int32, device=dev) for _ in range(G)]
     wts = [torch.empty((T, wl.k), dtype=torch.float32, device=dev) for _ in range(G)]
 
@@ -244,84 +341,37 @@ def run_ours(args, rank, world, local_rank):
 
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        for j in range(max(3, args.warmup)):
+        for j in range(max(3, warmup)):
             step(j, j % G)
     stream.synchronize()
     for L in layers:
         L.check()
 
-    # graphs: G steps each; a second graph for a remainder
-    def capture(n, offset):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for j in range(n):
-                step(offset + j, j)
-        return g
-
-    reps, rem = divmod(args.steps, G)
-    # the batched path has several kernels per call: time its stages with
-    # CUDA events recorded inside the graph (event-record nodes refreshed by
-    # every replay), so the dominant kernel's own duration is measured in the
-    # timed region
+    # the batched path has several kernels per call: its stages are timed
+    # with CUDA events recorded inside the graph (event-record nodes that
+    # every replay refreshes), so the dominant kernel's own duration is
+    # measured in the timed region
     staged = T > 8
     if staged:
         for L in layers:
             moe.moe_layer_enable_timing(L.handle, G)
-    launches0 = moe.moe_launch_count()
-    g_main = capture(G, 0) if reps else None
-    launches_per_graph = moe.moe_launch_count() - launches0
-    launches0 = moe.moe_launch_count()
-    g_rem = capture(rem, 0) if rem else None
-    launches_rem = moe.moe_launch_count() - launches0
-    with torch.cuda.stream(stream):
-        if g_main:
-            g_main.replay()
-        if g_rem:
-            g_rem.replay()
-    stream.synchronize()
-
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
-    with Clocks(local_rank) as clk:
-        with torch.cuda.stream(stream):
-            start.record(stream)
-            for i in range(reps):
-                g_main.replay()
-                marks[i].record(stream)
-            if g_rem:
-                g_rem.replay()
-            stop.record(stream)
-        stop.synchronize()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    ms = start.elapsed_time(stop)
+    ms, gpu_launches, clocks, pct = timed_graph_steps(torch, moe, stream, step, steps, G, local_rank, world)
     for L in layers:
         L.check()
     t_ms = torch.tensor([ms], device=dev)
     if world > 1:
         torch.distributed.all_reduce(t_ms, op=torch.distributed.ReduceOp.MAX)
     ms = float(t_ms.item())
-    steps = reps * G + rem
     stage_ms = None
-    if staged:  # per-stage means over the calls of the last replay(s)
+    if staged:  # per-stage means over the calls of the last replay
         rows = [r for L in layers for r in moe.moe_layer_stage_times(L.handle, G)]
-        stage_ms = {name: statistics.fmean(r[i] for r in rows) for i, name in enumerate(moe.STAGES)}
-        # the events stay bound to the graphs' nodes: drop both before any
-        # eager call on these layers
-        del g_main, g_rem
-        for L in layers:
+        stage_ms = {nm: statistics.fmean(r[i] for r in rows) for i, nm in enumerate(moe.STAGES)}
+        for L in layers:  # the events stay bound to the graphs: fresh ones before eager calls
             moe.moe_layer_enable_timing(L.handle, 0)
     ms_per_step = ms / steps
-    gpu_launches = reps * launches_per_graph + launches_rem
 
-    # distinct experts actually selected per step (for the byte count)
-    distinct = []
-    for s in range(min(G, steps)):
-        distinct.append(len(set(ids[s].flatten().tolist())))
+    # distinct experts selected per step (for the byte count)
+    distinct = [len(set(ids[s].flatten().tolist())) for s in range(min(G, steps))]
     mean_distinct = sum(distinct) / len(distinct)
     alg_bytes = algorithmic_bytes(wl, T, mean_distinct)
     expert_bytes = (mean_distinct + 1) * expert_bytes_of(wl)
@@ -329,13 +379,12 @@ def run_ours(args, rank, world, local_rank):
     # end to end through the public API with host buffers
     e2e = None
     if rank == 0:
-        n_e2e = max(1, min(args.e2e_steps, args.steps))
-        xh = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in xs_host]
-        oh = torch.empty((T, wl.H), dtype=torch.bfloat16).pin_memory()
+        n_e2e = max(1, min(args.e2e_steps, steps))
+        xh = [to_x(a).pin_memory() for a in xs_host]
+        oh = torch.empty((T, wl.H), dtype=xdt).pin_memory()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            # one C-ABI call per step: copy x in, run the layer, copy out back
-            for j in range(8):
+            for j in range(8):  # one C-ABI call per step: copy x in, run the layer, copy out back
                 moe.moe_layer_forward_routed_host(layers[j % NL].handle, xh[j % NX], routers[j % NL], ids[0],
                                                   wts[0], oh, bias)
             stream.synchronize()
@@ -346,81 +395,66 @@ def run_ours(args, rank, world, local_rank):
             e1.record(stream)
         e1.synchronize()
         e_ms = e0.elapsed_time(e1)
-        e2e = {"value": n_e2e * T / (e_ms / 1e3), "unit": "tokens/s",
-               "h2d_bytes_per_step": T * wl.H * 2, "d2h_bytes_per_step": T * wl.H * 2,
-               "steps": n_e2e}
+        nbytes = T * wl.H * (2 if wl.x_dtype == "bf16" else 4)
+        e2e = {"value": world * n_e2e * T / (e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": n_e2e,
+               "us_per_step": 1e3 * e_ms / n_e2e}
+    for L in layers:
+        L.check()
+        L.close()
+    del layers, routers, xs, outs, ids, wts
+    torch.cuda.empty_cache()
 
-    if rank != 0:
-        return
-    peaks = {}
-    try:
-        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-        hbm_peak, peak_src = float(peaks["hbm_gbs"]), "measured"
-    except (OSError, KeyError, ValueError):
-        hbm_peak, peak_src = 6800.0, "fallback"
     achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
-    tokens_per_s = world * T * steps / (ms / 1e3)
     roofline = {"bound": "hbm",
                 "kernel": ("decode_fused_kernel (the step's only launch)" if T <= 8
                            else "whole layer call (all launches of one step)"),
-                "achieved": achieved, "peak": hbm_peak, "peak_source": peak_src,
-                "unit": "GB/s", "frac": achieved / hbm_peak,
+                "achieved": achieved, "peak": pk["hbm"], "peak_source": pk["hbm_src"],
+                "unit": "GB/s", "frac": achieved / pk["hbm"],
                 "algorithmic_bytes_per_launch": alg_bytes,
-                "traffic": NCU_TRAFFIC.get(args.workload)}
+                "traffic": NCU_TRAFFIC.get(name) if T <= 8 else None}
+    out = {"value": world * T * steps / (ms / 1e3), "unit": "tokens/s", "steps": steps,
+           "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3, "config": cfg,
+           "expert_weight_gbs": expert_bytes / (ms_per_step * 1e-3) / 1e9,
+           "expert_weight_frac_of_hbm_peak": expert_bytes / (ms_per_step * 1e-3) / 1e9 / pk["hbm"],
+           "mean_distinct_experts": mean_distinct}
     if stage_ms and T >= 1024:
-        # dense contraction: the up/gate grouped GEMM against the tensor peak
-        # (fp16 operands; GB300's nominal fp16 and bf16 dense rates are equal,
-        # so the measured sustained bf16 cuBLAS rate is the fp16 peak)
+        # dense contraction: the up/gate grouped GEMM (a sub-millisecond
+        # kernel, so the burst bf16 peak; fp16 operands, and GB300's fp16 and
+        # bf16 dense rates are equal) against the tensor roofline, and the
+        # whole call's dense-equivalent flops beside it
         routes = T * (wl.k + 1)
         ug_flop = routes * 4.0 * wl.H * wl.F
-        try:
-            tc_peak, tc_src = float(peaks["bf16_tflops_sustained"]), "measured (sustained bf16 = fp16)"
-        except (KeyError, ValueError):
-            tc_peak, tc_src = 1700.0, "fallback"
         ug_tflops = ug_flop / (stage_ms["up/gate"] * 1e-3) / 1e12
+        out["hbm_roofline_of_call"] = roofline
         roofline = {"bound": "tensor", "kernel": "grouped_gemm_tc<up/gate>",
-                    "achieved": ug_tflops, "peak": tc_peak, "peak_source": tc_src,
-                    "unit": "TFLOP/s", "frac": ug_tflops / tc_peak,
+                    "achieved": ug_tflops, "peak": pk["bf16"], "peak_source": pk["bf16_src"] + " (fp16 = bf16 rate)",
+                    "unit": "TFLOP/s", "frac": ug_tflops / pk["bf16"],
                     "algorithmic_flops_per_launch": ug_flop,
-                    "launch_ms": stage_ms["up/gate"], "traffic": NCU_TRAFFIC.get(args.workload)}
-    line = {
-        "metric": METRIC,
-        "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": steps,
-        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in/out, IQ4_NL weights, fp32 accumulate",
-        "data": "synthetic (seeded; random IQ4_NL weights of the workload's layer shapes)",
-        "config": cfg,
-        "us_per_layer": ms_per_step * 1e3,
-        "expert_weight_gbs": expert_bytes / (ms_per_step * 1e-3) / 1e9,
-        "expert_weight_frac_of_hbm_peak": expert_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
-        "roofline": roofline,
-        "stage_ms": stage_ms,
-        "step_ms_percentiles": replay_percentiles(start, marks, G),
-        "gpu_launches": gpu_launches,
-        "clocks": clk.summary(),
-        "e2e": e2e,
-    }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
-    print(json.dumps(line), flush=True)
+                    "launch_ms": stage_ms["up/gate"], "traffic": NCU_TRAFFIC.get(name)}
+        call_tflops = layer_flops(wl, T) / (ms_per_step * 1e-3) / 1e12
+        out["whole_layer_tensor"] = {"achieved": call_tflops, "peak": pk["bf16"], "unit": "TFLOP/s",
+                                     "frac": call_tflops / pk["bf16"],
+                                     "flops_per_call": layer_flops(wl, T),
+                                     "peak_source": pk["bf16_src"]}
+    out.update({"roofline": roofline, "stage_ms": stage_ms, "step_ms_percentiles": pct,
+                "gpu_launches": gpu_launches, "clocks": clocks, "e2e": e2e})
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(name, cpu_seconds)
+    return out
 
 
-def run_trunk(args, rank, world, local_rank):
+def measure_trunk(args, name, steps, warmup, world, rank, local_rank, dev, cpu_seconds, headline):
     """A step is T tokens through the whole trunk: per layer a residual-add +
     RMSNorm launch and the layer's route + forward launches."""
     import numpy as np
     import torch
     import quantized_moe_expert_sigmoid_gb300 as moe
-    from quantized_moe_expert_sigmoid_gb300 import build as moe_build, synth
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if rank == 0 or not os.path.exists(moe_build.LIB):
-        moe_build.build()
-    if world > 1:
-        torch.distributed.barrier()
-    wl = synth.WORKLOADS[args.workload]
+    from quantized_moe_expert_sigmoid_gb300 import synth
+    wl = synth.WORKLOADS[name]
     T = wl.T
-    NL, NX, G, cfg = bench_config(args, wl, world)
+    NL, NX, G, cfg = bench_config(args, wl, world, steps)
+    pk = load_peaks()
     layers, routers = [], []
     for l in range(NL):
         ew = synth.expert_weights_torch(1000 * rank + 7, l, wl.E, wl.H, wl.F, device=dev)
@@ -435,55 +469,20 @@ def run_trunk(args, rank, world, local_rank):
     xs = [torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16) for a in xs_host]
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        for j in range(max(3, args.warmup)):
+        for j in range(max(3, warmup)):
             trunk.forward(xs[j % NX])
     stream.synchronize()
     trunk.check()
 
-    def capture(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for j in range(n):
-                trunk.forward(xs[j % NX])
-        return g
+    def step(j, slot):
+        trunk.forward(xs[j % NX])
 
-    reps, rem = divmod(args.steps, G)
-    launches0 = moe.moe_launch_count()
-    g_main = capture(G) if reps else None
-    launches_per_graph = moe.moe_launch_count() - launches0
-    launches0 = moe.moe_launch_count()
-    g_rem = capture(rem) if rem else None
-    launches_rem = moe.moe_launch_count() - launches0
-    with torch.cuda.stream(stream):
-        for g in (g_main, g_rem):
-            if g:
-                g.replay()
-    stream.synchronize()
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
-    with Clocks(local_rank) as clk:
-        with torch.cuda.stream(stream):
-            start.record(stream)
-            for i in range(reps):
-                g_main.replay()
-                marks[i].record(stream)
-            if g_rem:
-                g_rem.replay()
-            stop.record(stream)
-        stop.synchronize()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    ms = start.elapsed_time(stop)
+    ms, gpu_launches, clocks, pct = timed_graph_steps(torch, moe, stream, step, steps, G, local_rank, world)
     trunk.check()
     t_ms = torch.tensor([ms], device=dev)
     if world > 1:
         torch.distributed.all_reduce(t_ms, op=torch.distributed.ReduceOp.MAX)
     ms = float(t_ms.item())
-    steps = reps * G + rem
     ms_per_step = ms / steps
     # bytes of the last step: every layer's selected experts + shared, routers, activations
     distinct = [len(set(trunk.ids[l][:T].flatten().tolist())) for l in range(NL)]
@@ -492,7 +491,7 @@ def run_trunk(args, rank, world, local_rank):
 
     e2e = None
     if rank == 0:
-        n_e2e = max(1, min(args.e2e_steps, args.steps, 200))
+        n_e2e = max(1, min(args.e2e_steps, steps, 200))
         xh = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in xs_host]
         rh = torch.empty((T, wl.H), dtype=torch.float32).pin_memory()
         xd = torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev)
@@ -508,39 +507,68 @@ def run_trunk(args, rank, world, local_rank):
                 rh.copy_(trunk.forward(xd), non_blocking=True)
             e1.record(stream)
         e1.synchronize()
-        e2e = {"value": n_e2e * T / (e0.elapsed_time(e1) / 1e3), "unit": "tokens/s",
+        e2e = {"value": world * n_e2e * T / (e0.elapsed_time(e1) / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": T * wl.H * 2, "d2h_bytes_per_step": T * wl.H * 4,
                "steps": n_e2e}
+    for L in layers:
+        L.close()
+    del trunk, layers, routers, xs
+    torch.cuda.empty_cache()
+    achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
+    out = {"value": world * T * steps / (ms / 1e3), "unit": "tokens/s", "steps": steps,
+           "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3 / NL, "config": cfg,
+           "expert_weight_gbs": expert_bytes / (ms_per_step * 1e-3) / 1e9,
+           "expert_weight_frac_of_hbm_peak": expert_bytes / (ms_per_step * 1e-3) / 1e9 / pk["hbm"],
+           "expert_bytes_per_token": expert_bytes / T,
+           "step_ms_percentiles": pct,
+           "roofline": {"bound": "hbm", "kernel": f"whole trunk step ({NL} layers, all launches)",
+                        "achieved": achieved, "peak": pk["hbm"], "peak_source": pk["hbm_src"],
+                        "unit": "GB/s", "frac": achieved / pk["hbm"],
+                        "algorithmic_bytes_per_launch": alg_bytes, "traffic": None},
+           "gpu_launches": gpu_launches, "clocks": clocks, "e2e": e2e}
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(name, cpu_seconds)
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from quantized_moe_expert_sigmoid_gb300 import build as moe_build, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or not os.path.exists(moe_build.LIB):
+        moe_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+
+    def measure(name, steps, warmup, cpu_s, headline):
+        f = measure_trunk if synth.WORKLOADS[name].n_layers > 1 else measure_layer
+        return f(args, name, steps, warmup, world, rank, local_rank, dev, cpu_s, headline)
+
+    head = measure(args.workload, args.steps, args.warmup, args.cpu_seconds, True)
+    extra = {}
+    if world == 1 and not args.no_extra and args.workload == "decode1":
+        for name in EXTRA_WORKLOADS:
+            wl = synth.WORKLOADS[name]
+            # bounded: at least 20 steps, about a second of timed work each
+            n = max(20, min(args.steps, 200 if wl.T <= 64 and wl.n_layers == 1 else 40))
+            extra[name] = measure(name, n, max(3, min(args.warmup, 10)), min(args.cpu_seconds, 4.0), False)
     if rank != 0:
         return
-    try:
-        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-        hbm_peak, peak_src = float(peaks["hbm_gbs"]), "measured"
-    except (OSError, KeyError, ValueError):
-        hbm_peak, peak_src = 6800.0, "fallback"
-    achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
     line = {
         "metric": METRIC,
-        "value": world * T * steps / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
-        "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 in, fp32 residual, IQ4_NL weights, fp32 accumulate",
-        "data": "synthetic (seeded; random IQ4_NL weights of the Xing4 trunk shapes)",
-        "config": cfg,
-        "us_per_layer": ms_per_step * 1e3 / NL,
-        "expert_weight_gbs": expert_bytes / (ms_per_step * 1e-3) / 1e9,
-        "expert_weight_frac_of_hbm_peak": expert_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
-        "step_ms_percentiles": replay_percentiles(start, marks, G),
-        "roofline": {"bound": "hbm", "kernel": f"whole trunk step ({NL} layers, all launches)",
-                     "achieved": achieved, "peak": hbm_peak, "peak_source": peak_src,
-                     "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "algorithmic_bytes_per_launch": alg_bytes, "traffic": None},
-        "gpu_launches": reps * launches_per_graph + launches_rem,
-        "clocks": clk.summary(),
-        "e2e": e2e,
+        "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in/out, IQ4_NL weights, fp32 accumulate",
+        "data": "synthetic (seeded; random IQ4_NL weights of the workload's layer shapes)",
+        "config": head["config"],
     }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    for k, v in head.items():
+        if k not in ("value", "unit", "steps", "ms_per_step", "config"):
+            line[k] = v
+    if extra:
+        line["workloads"] = extra
     print(json.dumps(line), flush=True)
 
 
@@ -557,10 +585,7 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
     try:
-        if args.workload.startswith("trunk"):
-            run_trunk(args, rank, world, local_rank)
-        else:
-            run_ours(args, rank, world, local_rank)
+        run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch
