@@ -27,12 +27,31 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
  *     Route and forward calls are asynchronous on it; they never allocate,
  *     never synchronise and never copy data back to the host, so they can be
- *     captured in a CUDA graph.
+ *     captured in a CUDA graph.  (PocketLLM design record, section 6 "Where
+ *     a decode step's time goes": a route-count read back to the host cost a
+ *     copy and a stream drain per layer and was what refused graph capture.)
+ *   - Everything a call will need is sized and allocated when the layer is
+ *     created, and a shape the kernels cannot run is refused there, not in
+ *     the middle of a request (PocketLLM design record, section 5 "The
+ *     prefill chunk is a function of the card": a configuration that cannot
+ *     fit is a refusal at load rather than an out-of-memory error inside a
+ *     request).
  *   - Host-checkable errors (NULL pointer, bad size, T > max_tokens,
- *     misaligned base pointer) return a status and launch nothing.  Errors
- *     only the device can see (an expert id outside [0, E) handed to
- *     moe_forward, a device wait that gave up) set a sticky word in the layer
- *     that moe_layer_check() reports; the offending route contributes zero.
+ *     misaligned base pointer) return a status and launch nothing.  Base
+ *     pointers read with 16-byte vector loads are checked for 16-byte
+ *     alignment, not only their row strides (FLASHNEXT-RESEARCH.md, section
+ *     4 "Second target: 216 F32 GEMVs on a bare cuBLAS SGEMM": a guard that
+ *     checked the stride but not the base pointer of a float4-read operand
+ *     let an offset view fault).  Errors only the device can see (an expert
+ *     id outside [0, E) handed to moe_forward, a device wait that gave up)
+ *     set a sticky word in the layer that moe_layer_check() reports; the
+ *     offending route contributes zero.
+ *   - No call falls back to another implementation when its own cannot run:
+ *     it returns an error status (HelloSun/xing4_0-29b-IQ4_NL_EPQ model card,
+ *     "已知陷阱": fail loudly rather than quietly fall back to a different
+ *     path).  Where the layer has two GPU paths for a batch size (the
+ *     single-launch decode kernel and the tensor-core kernels), which one
+ *     runs is fixed at create from the shape and the device.
  *   - A layer is used by one stream at a time; separate layers are
  *     independent.
  */
@@ -122,8 +141,14 @@ typedef struct {
  * internal layout (same byte count: 8 blocks' scales and nibbles grouped in
  * 144-byte units, rows padded with zero blocks to a multiple of 256 weights
  * where H or F is not one) and allocates every workspace later calls need for
- * up to max_tokens tokens.  Runs on `stream` and synchronises it before
- * returning, so the caller may free its weight buffers afterwards.
+ * up to max_tokens tokens, so that no later call allocates or can run out of
+ * memory (PocketLLM design record, section 5: refuse at load, not inside a
+ * request).  The layer belongs to the device current at create; create also
+ * raises the kernels' shared-memory limits on that device and checks that the
+ * single-launch decode kernel's grid (one CTA per SM, with device-wide waits
+ * inside) can be resident all at once -- if not, batches of up to 8 tokens
+ * run on the tensor-core kernels instead.  Runs on `stream` and synchronises
+ * it before returning, so the caller may free its weight buffers afterwards.
  * On success *out holds the layer; on failure *out is NULL and nothing is
  * leaked. */
 moe_status moe_layer_create(const moe_shapes *shapes, const moe_weights *weights,
@@ -142,7 +167,10 @@ moe_status moe_layer_destroy(moe_layer_t layer);
  *               MOE_FLAG_SELECTION_BIAS to the sigmoid score for ranking only
  *   ids         [T][k] int32 out, descending score; equal scores -> lower id
  *   weights     [T][k] fp32 out, sum to routed_scaling per token
- * 0 <= T <= max_tokens; T == 0 returns MOE_OK and launches nothing. */
+ * 0 <= T <= max_tokens; T == 0 returns MOE_OK and launches nothing.
+ * The ids and weights stay on the device (PocketLLM design record, section
+ * 6: no route count is read back), ready for moe_forward on the same
+ * stream. */
 moe_status moe_route(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
                      const float *router_w, const float *logit_bias,
                      int64_t bias_row_stride, int32_t *ids, float *weights,
@@ -160,7 +188,15 @@ moe_status moe_route(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_
  * tokens the order of those additions is whatever order the atomics commit
  * in (up to k+1 terms per element), so outputs may differ in the last bits
  * between runs, unless the layer was created with MOE_FLAG_DETERMINISTIC;
- * up to 8 tokens every addition has a fixed order. */
+ * up to 8 tokens every addition has a fixed order.
+ * The per-expert histogram, prefix sum and permutation run on the device
+ * (PocketLLM design record, section 4: a CSR route table consumed by one
+ * grouped kernel; section 6: the counts are never read back), so the call
+ * is graph-capturable.  The single-launch decode kernel (T <= 8) holds every
+ * SM of the device for the duration of the call and waits device-wide
+ * inside: run no other kernel concurrently with it (other streams, MPS
+ * clients).  A grid that cannot become resident makes its bounded waits give
+ * up, and moe_layer_check() then reports MOE_ERR_TIMEOUT. */
 moe_status moe_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
                        const int32_t *ids, const float *weights, void *out,
                        moe_dtype out_dtype, void *stream);

@@ -278,3 +278,52 @@ def test_large_batch_router_bit_exact(H, E, k, T, zipf):
     np.testing.assert_array_equal(ids.cpu().numpy(), c.ids)
     np.testing.assert_allclose(w.cpu().numpy(), c.w, rtol=0, atol=2e-6)
     L.close()
+
+
+@pytest.mark.parametrize("T,boost", [(1, 2.0 ** 8), (3, 2.0 ** 15), (8, 2.0 ** 11)])
+def test_decode_activation_blocks_with_wide_range(T, boost):
+    """The single-launch decode kernel (T <= 8) holds x and the SwiGLU output
+    h as 16-bit integers with one power-of-two scale per 32-element block:
+    an element is exact while its exponent is within 6 of the block's
+    largest, and smaller ones are rounded to the block's step (at most 2^-14
+    of the block's largest).  Worst case for that reading of the
+    fp32-accumulating GEMV: one element of every 32-block scaled up by
+    2^8 .. 2^15 (so most of the block sits 8 to 15 binades below its
+    maximum), given routes, against the oracle within the parity tolerance."""
+    wl = synth.WORKLOADS["decode1"]
+    ew = parity.weights(0, 0, wl.E, wl.H, wl.F, 1)
+    c = cases.make_case(wl, T=T, ew=ew)
+    x32 = synth.bf16_bits_to_f32(c.x).reshape(T, wl.H // 32, 32).copy()
+    for t in range(T):
+        for b in range(wl.H // 32):
+            x32[t, b, (7 * t + 3 * b) % 32] *= boost * (1.0 if b % 2 else -1.0)
+    bits = synth.to_bf16_bits(x32.reshape(T, wl.H))
+    x64 = oracle.to_f64(bits, "bf16")
+    x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    L = _layer_for("decode1")
+    w32 = c.w.astype(np.float32)
+    out = L.forward(x, torch.from_numpy(c.ids).cuda(), torch.from_numpy(w32).cuda(), out_dtype=torch.float32)
+    L.check()
+    ref = oracle.moe_forward(x64, c.ids, w32.astype(np.float64), ew)
+    parity.assert_close_fp32(out.cpu().numpy(), ref, f"wide-range blocks T={T} boost 2^{int(np.log2(boost))}")
+
+
+def test_max_tokens_boundary():
+    """T == max_tokens runs; T == max_tokens + 1 is refused before any launch."""
+    import quantized_moe_expert_sigmoid_gb300 as moe
+    wl = synth.WORKLOADS["decode1"]
+    ew = parity.weights(0, 0, wl.E, wl.H, wl.F, 1)
+    c = cases.make_case(wl, T=9, ew=ew)
+    L = MoeLayer.from_weights(ew, k=wl.k, scale=wl.scale, max_tokens=8)
+    x, wr, _ = _dev_inputs(c)
+    out, ids, w = L.forward_routed(x[:8], wr, out_dtype=torch.float32)
+    L.check()
+    np.testing.assert_array_equal(ids.cpu().numpy(), c.ids[:8])
+    ref = oracle.moe_forward(c.x64[:8], c.ids[:8], c.w[:8], ew)
+    parity.assert_close_fp32(out.cpu().numpy(), ref, "T = max_tokens")
+    before = moe.moe_launch_count()
+    with pytest.raises(MoeError) as e:
+        L.forward_routed(x, wr)
+    assert e.value.name == "MOE_ERR_TOO_MANY_TOKENS"
+    assert moe.moe_launch_count() == before
+    L.close()
