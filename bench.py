@@ -77,9 +77,7 @@ METRIC = "MoE-layer tokens/s (expert-weight HBM GB/s as fraction of GB300 peak)"
 # from the ncu captures summarised in profiles/ (None when the kernel changed
 # after its capture).
 NCU_TRAFFIC = {
-    # decode_fused_kernel changed after its last ncu capture (31,980,544 B
-    # per launch then): null until it is captured again
-    "decode1": None,
+    "decode1": 31_969_536,        # decode_fused_kernel<1,7,64>, ncu dram read + write per launch
     "prefill4096": 457_219_328,   # grouped_gemm_tc<up/gate>, ncu dram read + write per launch
 }
 

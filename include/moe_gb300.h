@@ -194,9 +194,11 @@ moe_status moe_route(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_
  * grouped kernel; section 6: the counts are never read back), so the call
  * is graph-capturable.  The single-launch decode kernel (T <= 8) holds every
  * SM of the device for the duration of the call and waits device-wide
- * inside: run no other kernel concurrently with it (other streams, MPS
- * clients).  A grid that cannot become resident makes its bounded waits give
- * up, and moe_layer_check() then reports MOE_ERR_TIMEOUT. */
+ * inside, so it is launched as a cooperative launch: the runtime starts it
+ * only once its whole grid can be resident, and refuses it (MOE_ERR_CUDA,
+ * "too many blocks in cooperative launch") when the device cannot hold the
+ * grid at all.  Its waits are bounded as well; one that gives up is reported
+ * by moe_layer_check() as MOE_ERR_TIMEOUT. */
 moe_status moe_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
                        const int32_t *ids, const float *weights, void *out,
                        moe_dtype out_dtype, void *stream);
@@ -223,11 +225,16 @@ moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype 
                                     moe_dtype out_dtype, void *stream);
 
 /* moe_layer_forward_routed with x and out in host memory, for a layer
- * created with MOE_FLAG_HOST_IO: one call copies x (T * hidden elements of
- * x_dtype) into the layer's device buffer, runs the layer, and copies out
- * back, all enqueued on `stream` (cudaMemcpyAsync; x_host and out_host
- * should be page-locked for the copies to be asynchronous, and stay valid
- * and untouched until the stream has passed the call).  router_w,
+ * created with MOE_FLAG_HOST_IO: one call moves x (T * hidden elements of
+ * x_dtype) to the device, runs the layer, and moves out back, all enqueued
+ * on `stream`.  For batches of up to 8 tokens, when the device can address
+ * both host buffers directly (page-locked or registered memory, 16-byte
+ * aligned; on GB300 over the NVLink-C2C link to the Grace host), the
+ * single-launch decode kernel reads x and writes out through them and no
+ * copy is enqueued; otherwise x and out go through the layer's device
+ * buffers with cudaMemcpyAsync (page-locked buffers keep those copies
+ * asynchronous).  Either way x_host and out_host must stay valid and
+ * untouched until the stream has passed the call.  router_w,
  * logit_bias, ids and weights are device pointers as for
  * moe_layer_forward_routed.  MOE_ERR_INVALID_ARG for a layer without the
  * flag or a NULL host pointer; otherwise errors as for

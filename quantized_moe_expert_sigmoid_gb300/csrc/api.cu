@@ -69,6 +69,18 @@ bool is_device_ptr(const void *p) {
   return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
+// Device address of a host buffer the device can read and write directly
+// (page-locked or registered memory), or nullptr.
+void *device_view(const void *host) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost) return nullptr;
+  return a.devicePointer;
+}
+
 void free_layer(Layer *L) {
   if (!L) return;
   void *ptrs[] = {L->gu, L->dn, L->logits, L->offsets, L->active, L->route_token,
@@ -162,7 +174,12 @@ moe_status forward_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const
   if (!L->deterministic)
     MOE_CUDA(cudaMemsetAsync(L->out_acc, 0, sizeof(float) * (size_t)T * L->H, st), "clear accumulator");
   MOE_CUDA(moe::launch_route_plan(*L, ids, w, T, st), "route plan");
-  MOE_CUDA(moe::launch_prefill_tc(*L, x, xdt, T, st, ev ? ev + 1 : nullptr), "tensor-core expert GEMMs");
+  if (moe::gemv_mma_supported(*L, T)) {
+    MOE_CUDA(moe::launch_gather_x16(*L, x, xdt, T, st), "gather");
+    MOE_CUDA(moe::launch_gemv_mma(*L, st, ev ? ev + 1 : nullptr), "batched decode expert GEMVs");
+  } else {
+    MOE_CUDA(moe::launch_prefill_tc(*L, x, xdt, T, st, ev ? ev + 1 : nullptr), "tensor-core expert GEMMs");
+  }
   if (L->deterministic)
     MOE_CUDA(moe::launch_combine_ordered(*L, T, out, odt, st), "ordered combine");
   else
@@ -314,6 +331,7 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
     if (e == cudaSuccess) e = moe::launch_repack(down, H, F, dn, L->dn_row_bytes, 0, 0, st);
   }
   if (e == cudaSuccess) e = moe::tc_prepare(*L);
+  if (e == cudaSuccess) e = moe::gemv_prepare(*L);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {
     free_layer(L);
@@ -423,6 +441,16 @@ moe_status moe_layer_forward_routed_host(moe_layer_t layer, const void *x_host, 
   if (!x_host || !out_host) return fail(MOE_ERR_INVALID_ARG, "x_host and out_host must be non-NULL");
   cudaStream_t st = (cudaStream_t)stream;
   const size_t n = (size_t)T * L->H;
+  // Batches the single-launch decode kernel runs read x and write out
+  // through the host buffers themselves when the device can address them
+  // (page-locked memory; on GB300 over the NVLink-C2C link to the Grace
+  // host), so a step is one launch and no copy-engine round trips.
+  if (moe::fused_decode_supported(*L, T)) {
+    void *xd = device_view(x_host), *od = device_view(out_host);
+    if (xd && od && moe::aligned(xd, 16) && moe::aligned(od, 16))
+      return moe_layer_forward_routed(layer, xd, x_dtype, T, router_w, logit_bias, bias_row_stride, ids,
+                                      weights, od, out_dtype, stream);
+  }
   MOE_CUDA(cudaMemcpyAsync(L->x_stage, x_host, n * (x_dtype == MOE_DT_BF16 ? 2 : 4), cudaMemcpyHostToDevice, st),
            "copy x to the device");
   const moe_status s = moe_layer_forward_routed(layer, L->x_stage, x_dtype, T, router_w, logit_bias,

@@ -958,11 +958,17 @@ cudaError_t launch_tt(const Params &p, int grid, size_t smem, cudaStream_t strea
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  // cooperative: the runtime refuses the launch (cudaErrorCooperativeLaunchTooLarge)
+  // unless every CTA of the grid can be resident at once, which the
+  // device-wide waits inside need; programmatic serialization: the next
+  // call's prologue overlaps this call's tail
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, decode_fused_kernel<TT, NP, NPD>, p);
 }
 
