@@ -226,8 +226,10 @@ int oracle_moe_forward(int64_t T, int64_t H, int64_t E, int64_t k, int64_t F,
   double *wg = (double *)malloc(sizeof(double) * (size_t)(F * H));
   double *wd = (double *)malloc(sizeof(double) * (size_t)(H * F));
   double *h = (double *)malloc(sizeof(double) * (size_t)F);
-  int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * (size_t)T);
-  double *wt = (double *)malloc(sizeof(double) * (size_t)T);
+  /* an expert may be named in several slots of one token, so it can hold up
+   * to T * k routes (and the shared expert T <= T * k) */
+  int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * (size_t)(T * k));
+  double *wt = (double *)malloc(sizeof(double) * (size_t)(T * k));
 
   for (int64_t e = 0; e < E + n_shared; ++e) {
     const int shared = (e == E);

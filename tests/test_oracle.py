@@ -249,6 +249,22 @@ def pin_zero_weight_route_contributes_nothing():
     assert np.allclose(out, want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
 
 
+def pin_repeated_expert_in_one_token():
+    # out[t] sums w * FFN over the slots, so an expert named in every slot of
+    # a token contributes (sum of its weights) * FFN_e once per token; four
+    # tokens with three slots each put twelve routes on one expert
+    ew, wr, x = _tiny_layer(seed=11)
+    x = np.concatenate([x, x[:1] * 0.5])
+    ids = np.array([[2, 2, 2], [6, 6, 6], [2, 2, 2], [6, 2, 6]], dtype=np.int32)
+    w = np.array([[0.5, 0.25, 1.0], [1.0, 0.5, 0.5], [0.125, 0.125, 0.25], [0.75, 1.5, 0.25]])
+    out = oracle.moe_forward(x, ids, w, ew)
+    f = lambda e, t: _dense_ffn(ew.up[e], ew.gate[e], ew.down[e], x[t])
+    sh = lambda t: _dense_ffn(ew.sh_up, ew.sh_gate, ew.sh_down, x[t])
+    want = np.stack([1.75 * f(2, 0) + sh(0), 2.0 * f(6, 1) + sh(1), 0.5 * f(2, 2) + sh(2),
+                     1.0 * f(6, 3) + 1.5 * f(2, 3) + sh(3)])
+    assert np.allclose(out, want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
+
+
 def pin_rmsnorm_closed_form():
     r = np.array([[3.0] * 8, [-0.5] * 8, [0.0] * 8])
     u = oracle.rmsnorm(r, 1e-6)
@@ -317,7 +333,7 @@ PINS = [pin_fp16_values, pin_golden_blocks, pin_matrix_bytes, pin_roundtrip,
         pin_router_hand_case, pin_router_brute_force, pin_weights_sum_to_scale,
         pin_rank_one_closed_form, pin_all_experts_equals_dense, pin_top1_special_case,
         pin_permutation_and_token_independence, pin_zero_weight_route_contributes_nothing,
-        pin_rmsnorm_closed_form, pin_invalid_ids_rejected, pin_selection_bias_hand_case,
+        pin_repeated_expert_in_one_token, pin_rmsnorm_closed_form, pin_invalid_ids_rejected, pin_selection_bias_hand_case,
         pin_selection_bias_zero_and_forcing, pin_dense_block]
 
 
