@@ -171,8 +171,7 @@ moe_status forward_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const
     }
     return MOE_OK;
   }
-  if (!L->deterministic)
-    MOE_CUDA(cudaMemsetAsync(L->out_acc, 0, sizeof(float) * (size_t)T * L->H, st), "clear accumulator");
+  // (the gather below also clears the fp32 output accumulator)
   MOE_CUDA(moe::launch_route_plan(*L, ids, w, T, st), "route plan");
   if (moe::gemv_mma_supported(*L, T)) {
     MOE_CUDA(moe::launch_gather_x16(*L, x, xdt, T, st), "gather");

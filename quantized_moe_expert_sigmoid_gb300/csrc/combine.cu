@@ -13,6 +13,7 @@
 // in slot order, the shared expert last, then one rounding.  Dropped routes
 // (an invalid id, pos -1) add nothing.  Every step has a fixed order, so
 // equal inputs give equal bits.
+#include "device_utils.cuh"
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -33,6 +34,8 @@ __device__ __forceinline__ void store4(void *out, int64_t i4, float4 v, int bf16
 
 __global__ void finalize_kernel(const float *__restrict__ acc, int64_t n, void *out, int bf16) {
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  pdl_wait();  // the accumulator comes from the previous launch
+  pdl_launch_dependents();
   if (i * 4 >= n) return;
   store4(out, i, *reinterpret_cast<const float4 *>(acc + i * 4), bf16);  // n is a multiple of 32
 }
@@ -44,6 +47,8 @@ __global__ void combine_ordered_kernel(const float *__restrict__ ybuf, const int
                                        int H, int Hp, void *out, int bf16) {
   const int h4 = H / 4;
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  pdl_wait();  // the per-route rows come from the previous launch
+  pdl_launch_dependents();
   if (i >= (int64_t)T * h4) return;
   const int t = (int)(i / h4), c = (int)(i % h4) * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -83,20 +88,18 @@ cudaError_t launch_fill(float *dst, float value, int n, cudaStream_t stream) {
 cudaError_t launch_finalize(const Layer &L, int T, void *out, moe_dtype odt, cudaStream_t stream) {
   const int64_t n = (int64_t)T * L.H;
   const int64_t threads = n / 4;
-  finalize_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(L.out_acc, n, out,
-                                                                         odt == MOE_DT_BF16);
-  count_launches(1);
-  return cudaGetLastError();
+  return count_and_check(launch_pdl(finalize_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0,
+                                    stream, (const float *)L.out_acc, n, out, odt == MOE_DT_BF16 ? 1 : 0));
 }
 
 cudaError_t launch_combine_ordered(const Layer &L, int T, void *out, moe_dtype odt,
                                    cudaStream_t stream) {
   if (!L.ybuf || !L.route_pos) return cudaErrorInvalidValue;
   const int64_t threads = (int64_t)T * (L.H / 4);
-  combine_ordered_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(
-      L.ybuf, L.route_pos, L.offsets, T, L.k, L.E, L.S, L.H, L.Hp, out, odt == MOE_DT_BF16);
-  count_launches(1);
-  return cudaGetLastError();
+  return count_and_check(launch_pdl(combine_ordered_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256),
+                                    0, stream, (const float *)L.ybuf, (const int *)L.route_pos,
+                                    (const int *)L.offsets, T, L.k, L.E, L.S, L.H, L.Hp, out,
+                                    odt == MOE_DT_BF16 ? 1 : 0));
 }
 
 }  // namespace moe

@@ -34,6 +34,8 @@ constexpr int kGroupRows = 64;  // gate/up interleave group
 
 // Largest batch the single-launch decode kernel handles.
 constexpr int kFusedMaxTokens = 8;
+// Largest batch of the batched decode path (register dequantisation + mma.sync).
+constexpr int kGemvMaxTokens = 64;
 constexpr int kLogitCopies = 8;  // copies of the decode kernel's tagged router logits
 
 // Sticky device error bits (Layer::err).
@@ -105,7 +107,32 @@ struct Layer {
   CUtensorMap map_x16, map_h16;        // activation tiles of the tensor-core path (256 rows)
   CUtensorMap map_x16_64, map_h16_64;  // ... boxes of 64 rows, for batches of <= 64 tokens
   CUtensorMap map_gu_lab, map_dn_lab;  // weight labels of one k-step
+  // batched decode path (9..64 tokens)
+  CUtensorMap map_gu_sb, map_dn_sb;    // one superblock column of 128 weight rows
+  CUtensorMap map_x16_16, map_h16_16;  // activation rows in route order, 16-row boxes
+  int gemv_ready = 0;                  // the layer's shape fits the batched decode path
 };
+
+// Launch with programmatic dependent launch allowed: the kernel may be
+// scheduled while the previous kernel in the stream is still running, so its
+// launch latency overlaps that kernel's tail.  Every kernel launched this way
+// executes griddepcontrol.wait (pdl_wait) before it touches memory that an
+// earlier launch writes or reads, and lets its own dependents launch early.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
 
 // Records the detail string behind moe_last_error() for the calling thread
 // and returns `s` (printf-style).
@@ -113,6 +140,12 @@ moe_status report_error(moe_status s, const char *fmt, ...);
 
 // Launch counter behind moe_launch_count(); every launcher adds its kernels.
 void count_launches(int n);
+
+// One launch counted; the launch's own error, else any pending one.
+inline cudaError_t count_and_check(cudaError_t e) {
+  count_launches(1);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 // Alignment helper.
 inline bool aligned(const void *p, uintptr_t a) {
@@ -186,6 +219,17 @@ cudaError_t tc_prepare(Layer &L);  // tensor maps + kernel attributes (after wor
 // ev: nullable; the events to record before up/gate, after up/gate and after down
 cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int T, cudaStream_t stream,
                               cudaEvent_t *ev = nullptr);
+
+// gemv_mma.cu: batched decode path for kFusedMaxTokens < T <= kGemvMaxTokens
+// (up/gate + SwiGLU into h16, then down into out_acc or ybuf), after the
+// route plan and gather_x16.  ev: nullable, as for launch_prefill_tc.
+bool gemv_mma_supported(const Layer &L, int T);
+cudaError_t gemv_prepare(Layer &L);  // tensor maps + kernel attributes (create)
+cudaError_t launch_gemv_mma(const Layer &L, cudaStream_t stream, cudaEvent_t *ev = nullptr);
+// prefill_tc.cu: x rows in route order as fp16 (x16)
+// Also clears the fp32 output accumulator (T x H) unless the layer combines
+// deterministically (the batched paths add into it with atomics).
+cudaError_t launch_gather_x16(const Layer &L, const void *x, moe_dtype xdt, int T, cudaStream_t stream);
 
 // norm.cu
 cudaError_t launch_residual_rmsnorm(float *resid, const void *delta, moe_dtype ddt,

@@ -4,6 +4,7 @@
 //   resid[t] += delta[t];  u[t] = bf16(resid[t] / sqrt(mean(resid[t]^2) + eps))
 // One CTA per token, 8 elements per thread per step, fp32 throughout, one
 // round-to-nearest-even to bf16 at the end.
+#include "device_utils.cuh"
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -33,6 +34,8 @@ __global__ void __launch_bounds__(256) residual_rmsnorm_kernel(float *__restrict
                                                                __nv_bfloat16 *__restrict__ u) {
   __shared__ float red[8];
   const int t = blockIdx.x;
+  pdl_wait();  // the residual and the layer output come from earlier launches
+  pdl_launch_dependents();
   float *r = resid + (int64_t)t * H;
   float ss = 0.f;
   for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
@@ -75,13 +78,10 @@ cudaError_t launch_residual_rmsnorm(float *resid, const void *delta, moe_dtype d
                                     int T, int H, float eps, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   if (ddt == MOE_DT_BF16)
-    residual_rmsnorm_kernel<__nv_bfloat16><<<T, 256, 0, stream>>>(
-        resid, (const __nv_bfloat16 *)delta, H, eps, (__nv_bfloat16 *)u);
-  else
-    residual_rmsnorm_kernel<float><<<T, 256, 0, stream>>>(resid, (const float *)delta, H, eps,
-                                                          (__nv_bfloat16 *)u);
-  count_launches(1);
-  return cudaGetLastError();
+    return count_and_check(launch_pdl(residual_rmsnorm_kernel<__nv_bfloat16>, dim3(T), dim3(256), 0, stream,
+                                      resid, (const __nv_bfloat16 *)delta, H, eps, (__nv_bfloat16 *)u));
+  return count_and_check(launch_pdl(residual_rmsnorm_kernel<float>, dim3(T), dim3(256), 0, stream, resid,
+                                    (const float *)delta, H, eps, (__nv_bfloat16 *)u));
 }
 
 }  // namespace moe

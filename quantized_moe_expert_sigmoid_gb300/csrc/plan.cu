@@ -22,6 +22,7 @@
 // tensor-core path (route tiles of <= 256 per expert -- <= 64 for batches of
 // up to 64 tokens -- and every weight tile of each), from the offsets it
 // holds in shared memory.
+#include "device_utils.cuh"
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -61,6 +62,8 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(
   const int r_beg = warp * chunk;
   const int r_end = min(R, r_beg + chunk);
   const unsigned lt_mask = (1u << lane) - 1u;
+  pdl_wait();  // the routes come from the previous launch
+  pdl_launch_dependents();
 
   for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
@@ -208,14 +211,11 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(
 
 cudaError_t launch_route_plan(const Layer &L, const int32_t *ids, const float *weights, int T,
                               cudaStream_t stream) {
-  route_plan_kernel<<<1, 1024, 0, stream>>>(ids, weights, T, L.k, L.E, L.S, L.offsets, L.active,
-                                            L.route_token, L.route_weight, L.err, L.tiles_ug,
-                                            L.tiles_dn, L.tile_counts, L.Fp / 128, L.Hp / 256,
-                                            tc_max_tiles(L, true), tc_max_tiles(L, false),
-                                            L.deterministic ? L.route_pos : nullptr,
-                                            tc_tile_routes(T));
-  count_launches(1);
-  return cudaGetLastError();
+  return count_and_check(launch_pdl(route_plan_kernel, dim3(1), dim3(1024), 0, stream, ids, weights, T, L.k,
+                                    L.E, L.S, L.offsets, L.active, L.route_token, L.route_weight, L.err,
+                                    L.tiles_ug, L.tiles_dn, L.tile_counts, L.Fp / 128, L.Hp / 256,
+                                    tc_max_tiles(L, true), tc_max_tiles(L, false),
+                                    L.deterministic ? L.route_pos : nullptr, tc_tile_routes(T)));
 }
 
 }  // namespace moe

@@ -404,10 +404,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 template <typename XT>
 __global__ void gather_x16_kernel(const XT *__restrict__ x, const int *__restrict__ route_token,
                                   const int *__restrict__ total, int H, int Hp, int max_rows,
-                                  __half *__restrict__ x16, unsigned *err) {
+                                  __half *__restrict__ x16, unsigned *err, float4 *__restrict__ zero,
+                                  unsigned zero_n4) {
   // one 8-element chunk; the launcher keeps max_rows * Hp / 8 below 2^32, so
   // the row split is a 32-bit division (a 64-bit one is a long sequence)
   const unsigned i = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();  // the route plan (and x) come from earlier launches
+  pdl_launch_dependents();
+  // clear the output accumulator of the batched paths (grid-stride; the
+  // grid has a thread per chunk, more than the accumulator's float4s)
+  if (zero)
+    for (unsigned j = i; j < zero_n4; j += gridDim.x * blockDim.x) zero[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   const unsigned hp8 = (unsigned)Hp / 8u;
   const int row = (int)(i / hp8);
   const int c8 = (int)(i % hp8);
@@ -530,22 +537,28 @@ cudaError_t tc_prepare(Layer &L) {
   return e;
 }
 
-cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int T,
-                              cudaStream_t stream, cudaEvent_t *ev) {
+cudaError_t launch_gather_x16(const Layer &L, const void *x, moe_dtype xdt, int T, cudaStream_t stream) {
   const int max_rows = T * L.k + L.S * T;
-  cudaError_t e;
-  // gather x in route order as fp16
   const int64_t chunks = (int64_t)max_rows * (L.Hp / 8);
   if (chunks + 255 >= ((int64_t)1 << 32)) return cudaErrorInvalidValue;  // 32-bit chunk index
   const int gb = (int)((chunks + 255) / 256);
+  float4 *zero = L.deterministic ? nullptr : reinterpret_cast<float4 *>(L.out_acc);
+  const unsigned zero_n4 = (unsigned)((int64_t)T * L.H / 4);  // H is a multiple of 32
   if (xdt == MOE_DT_BF16)
-    gather_x16_kernel<__nv_bfloat16><<<gb, 256, 0, stream>>>(
-        (const __nv_bfloat16 *)x, L.route_token, L.offsets + L.E + L.S, L.H, L.Hp, max_rows, L.x16, L.err);
-  else
-    gather_x16_kernel<float><<<gb, 256, 0, stream>>>((const float *)x, L.route_token, L.offsets + L.E + L.S,
-                                                     L.H, L.Hp, max_rows, L.x16, L.err);
-  count_launches(1);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return count_and_check(launch_pdl(gather_x16_kernel<__nv_bfloat16>, dim3(gb), dim3(256), 0, stream,
+                                      (const __nv_bfloat16 *)x, (const int *)L.route_token,
+                                      (const int *)(L.offsets + L.E + L.S), L.H, L.Hp, max_rows, L.x16, L.err,
+                                      zero, zero_n4));
+  return count_and_check(launch_pdl(gather_x16_kernel<float>, dim3(gb), dim3(256), 0, stream, (const float *)x,
+                                    (const int *)L.route_token, (const int *)(L.offsets + L.E + L.S), L.H,
+                                    L.Hp, max_rows, L.x16, L.err, zero, zero_n4));
+}
+
+cudaError_t launch_prefill_tc(const Layer &L, const void *x, moe_dtype xdt, int T,
+                              cudaStream_t stream, cudaEvent_t *ev) {
+  cudaError_t e;
+  // gather x in route order as fp16
+  if ((e = launch_gather_x16(L, x, xdt, T, stream)) != cudaSuccess) return e;
 
   TcParams p;
   p.route_token = L.route_token;

@@ -20,6 +20,7 @@
 
 #include <mutex>
 
+#include "device_utils.cuh"
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -54,6 +55,8 @@ __global__ void __launch_bounds__(256) router_logits_small(const XT *__restrict_
                                                            float *__restrict__ logits) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + warp;
+  pdl_wait();  // x may come from the previous launch
+  pdl_launch_dependents();
   if (e >= E) return;
   const float *w = wr + (int64_t)e * H;
   for (int t0 = 0; t0 < T; t0 += kSmallTokens) {
@@ -116,6 +119,8 @@ __global__ void __launch_bounds__(256) router_logits_tiled(const XT *__restrict_
   const XT *xp = x + (int64_t)(t0 + lt) * H + lk;
   const float *wp = wr + (int64_t)(e0 + le) * H + lw;
   const int kb = blockIdx.z * kc, ke = min(H, kb + kc);
+  pdl_wait();  // x may come from the previous launch
+  pdl_launch_dependents();
   logits += (int64_t)blockIdx.z * T * E;
   if (blockIdx.z != 0) bias = nullptr;
   float4 xr = make_float4(0.f, 0.f, 0.f, 0.f), wr0 = xr, wr1 = xr;
@@ -191,6 +196,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
                                                           float *__restrict__ weights) {
   const int lane = threadIdx.x & 31;
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  pdl_wait();  // the logits come from the previous launch
+  pdl_launch_dependents();
   if (t >= T) return;
   // selection key per expert: the biased logit (logit mode), or the sigmoid
   // score plus the bias (selection mode, whose weights use the plain score)
@@ -277,23 +284,22 @@ cudaError_t launch_router_logits(const Layer &L, const void *x, moe_dtype xdt, i
   if (T <= 16) {
     dim3 grid((L.E + 7) / 8);
     if (xdt == MOE_DT_BF16)
-      router_logits_small<__nv_bfloat16><<<grid, 256, 0, stream>>>(
-          (const __nv_bfloat16 *)x, T, L.H, wr, L.E, bias, bias_stride, logits);
+      return count_and_check(launch_pdl(router_logits_small<__nv_bfloat16>, grid, dim3(256), 0, stream,
+                                        (const __nv_bfloat16 *)x, T, L.H, wr, L.E, bias, bias_stride, logits));
     else
-      router_logits_small<float><<<grid, 256, 0, stream>>>((const float *)x, T, L.H, wr, L.E,
-                                                           bias, bias_stride, logits);
+      return count_and_check(launch_pdl(router_logits_small<float>, grid, dim3(256), 0, stream, (const float *)x,
+                                        T, L.H, wr, L.E, bias, bias_stride, logits));
   } else {
     const int kc = ((L.H + parts - 1) / parts + kKC - 1) / kKC * kKC;
     dim3 grid((T + kTM - 1) / kTM, (L.E + kTN - 1) / kTN, parts);
     if (xdt == MOE_DT_BF16)
-      router_logits_tiled<__nv_bfloat16><<<grid, 256, 0, stream>>>(
-          (const __nv_bfloat16 *)x, T, L.H, wr, L.E, bias, bias_stride, kc, logits);
+      return count_and_check(launch_pdl(router_logits_tiled<__nv_bfloat16>, grid, dim3(256), 0, stream,
+                                        (const __nv_bfloat16 *)x, T, L.H, wr, L.E, bias, bias_stride, kc,
+                                        logits));
     else
-      router_logits_tiled<float><<<grid, 256, 0, stream>>>((const float *)x, T, L.H, wr, L.E,
-                                                           bias, bias_stride, kc, logits);
+      return count_and_check(launch_pdl(router_logits_tiled<float>, grid, dim3(256), 0, stream, (const float *)x,
+                                        T, L.H, wr, L.E, bias, bias_stride, kc, logits));
   }
-  count_launches(1);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_router_topk(const Layer &L, const float *logits, int parts, const float *bias,
@@ -301,10 +307,9 @@ cudaError_t launch_router_topk(const Layer &L, const float *logits, int parts, c
                                cudaStream_t stream) {
   const int warps_per_block = 8;
   const int blocks = (T + warps_per_block - 1) / warps_per_block;
-  router_topk_kernel<<<blocks, 32 * warps_per_block, 0, stream>>>(logits, parts, bias, bias_stride, T,
-                                                                  L.E, L.k, L.scale, L.sel_bias, ids, weights);
-  count_launches(1);
-  return cudaGetLastError();
+  return count_and_check(launch_pdl(router_topk_kernel, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
+                                    logits, parts, bias, bias_stride, T, L.E, L.k, L.scale, L.sel_bias, ids,
+                                    weights));
 }
 
 }  // namespace moe
