@@ -127,6 +127,44 @@ __device__ __noinline__ void issue_copy(const Item it, int eid, uint8_t *dst, ui
   }
 }
 
+// W_down units of every remaining expert at one token, in one pass (see the
+// down phase of decode_fused_kernel): NU live (row, 16-weight) units per
+// thread, rows ct / NPD + (kConsumers / NPD) m, position ct % NPD.
+template <int NPD, int NU, int TT>
+__device__ __forceinline__ void down_units_t1(const Item *its, int n_rem, const uint8_t *ring, const int *ex_rs,
+                                              const int8_t (*rid)[kFusedMaxTokens], const int16_t *hq,
+                                              const float *shs, int grp_rs, int ct, int i0, int nst,
+                                              float (&acc)[kUnits][TT]) {
+  constexpr int kFp = NPD * 16, kDb = NPD / 16 * kSBBytes, kRowStep = kConsumers / NPD;
+  const int pos = ct & (NPD - 1), b = pos >> 1;
+  const int wofs = (b >> 3) * kSBBytes + 16 + (b & 7) * 16 + (pos & 1) * 8;
+  const int dofs = (b >> 3) * kSBBytes + (b & 7) * 2;
+#pragma unroll 2
+  for (int j = 0; j < n_rem; ++j) {
+    const Item itj = its[j];
+    const int r = rid[itj.a][0];
+    if (r < 0) continue;
+    const int ho = ex_rs[itj.a] - grp_rs + r;
+    const int16_t *hr = hq + ho * kFp + pos * 16;
+    const uint4 ha = *reinterpret_cast<const uint4 *>(hr);
+    const uint4 hb2 = *reinterpret_cast<const uint4 *>(hr + 8);
+    const float sh = shs[ho * (kFp / 32) + b];
+    const int stg = nst == 6 ? (i0 + j) % 6 : (i0 + j) % 3;
+    const uint8_t *st = ring + (size_t)stg * kStage + (ct / NPD) * kDb;
+#pragma unroll
+    for (int m = 0; m < NU; ++m) {
+      const uint2 q = *reinterpret_cast<const uint2 *>(st + kRowStep * kDb * m + wofs);
+      const float d = __half2float(*reinterpret_cast<const __half *>(st + kRowStep * kDb * m + dofs));
+      uint32_t c0, c1, c2, c3;
+      iq4_decode8(q.x, c0, c1);
+      iq4_decode8(q.y, c2, c3);
+      const int s0 = dot8_dp2a(c0, c1, ha, 0);
+      const int s1 = dot8_dp2a(c2, c3, hb2, 0);
+      acc[m][0] = fmaf((float)(s0 + s1), d * sh, acc[m][0]);
+    }
+  }
+}
+
 // NP > 0: rows of Hp = NP * 512 weights (NP 16-weight positions per lane),
 // at most 64 experts, bf16 x; NPD > 0: W_down rows of Fp = NPD * 16 weights.
 // With both known at compile time every shared-memory offset in the inner
@@ -247,8 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
     if (do_route && p.wr_rows_smem == 0)
       for (int e = c; e < E; e += G)
         for (int i = lane * 32; i < H; i += 32 * 32) prefetch_l2(p.wr + (int64_t)e * H + i);
-    pdl_wait();
 
+    pdl_wait();
     bool ok = true;
     {
       // ---- top-k of every token (every CTA computes the same selection) ----
@@ -276,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
               }
             }
             have = __all_sync(0xffffffffu, mine);
-            if (!have) __nanosleep(384);
+            if (!have) __nanosleep(128);
           }
           if (!have) {
             ok = false;
@@ -458,7 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
       int i = issued;
       for (; i < n_items; ++i) {
         const int s = stage_of(i);  // a stage's first use needs no wait
-        if (i >= nst && !mbar_wait_suspend(&empty_bar[s], (uint32_t)(round_of(i) - 1) & 1u, kWaitNs)) {
+        // a spinning wait: a suspended one wakes up late, and every copy
+        // issued late is a copy the consumers wait for
+        if (i >= nst && !mbar_wait_ns(&empty_bar[s], (uint32_t)(round_of(i) - 1) & 1u, kWaitNs)) {
           atomicOr(&status, 2);
           break;
         }
@@ -762,6 +802,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const Params 
           grp_end = ge;
           grp_rs = rs;
           named_sync(kBarConsumers, kConsumers);
+        }
+        if constexpr (TT == 1 && NPD > 0) {
+          // One token, and every remaining expert's h staged with its W_down
+          // rows in the ring at once (the ring holds them all): one pass over
+          // all of them, so a thread's units of every expert are independent
+          // work in flight together instead of one item after another.
+          const int n_rem = n_items - i;
+          if (grp_end >= n_ex && n_rem <= nst) {
+            for (int j = 0; j < n_rem; ++j)
+              if (!mbar_wait_ns(&full_bar[stage_of(i + j)], (uint32_t)round_of(i + j) & 1u, kWaitNs))
+                atomicOr(&status, 2);
+            // this warp's units (rows ct / NPD + 12 m) that exist: a warp-uniform count,
+            // so only live units are issued
+            const int r0u = ct / NPD, cnt = items[i].count;
+            constexpr int kRowStep = kConsumers / NPD;
+            const int nu = r0u + 2 * kRowStep < cnt ? 3 : r0u + kRowStep < cnt ? 2 : r0u < cnt ? 1 : 0;
+            if (nu == 2)
+              down_units_t1<NPD, 2>(items + i, n_rem, ring, ex_rs, rid, hq, shs, grp_rs, ct, i, nst, acc);
+            else if (nu == 3)
+              down_units_t1<NPD, 3>(items + i, n_rem, ring, ex_rs, rid, hq, shs, grp_rs, ct, i, nst, acc);
+            else if (nu == 1)
+              down_units_t1<NPD, 1>(items + i, n_rem, ring, ex_rs, rid, hq, shs, grp_rs, ct, i, nst, acc);
+            __syncwarp();
+            if (lane == 0)
+              for (int j = 0; j < n_rem; ++j) mbar_arrive(&empty_bar[stage_of(i + j)]);
+            i = n_items;
+            break;
+          }
         }
         const int hoff = rs - grp_rs;
         const int s = stage_of(i);
