@@ -137,7 +137,7 @@ moe_status route_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const f
     parts = moe::router_tc_parts(*L, T);
     MOE_CUDA(moe::launch_router_tc(*L, x, T, wr, L->logits, parts, st), "router logits");
   } else {
-    parts = moe::router_parts(T, moe::kRouterMaxParts);
+    parts = moe::router_parts(T, L->E, L->H, L->sms, 1 << 30);
     MOE_CUDA(moe::launch_router_logits(*L, x, xdt, T, wr, L->logits, parts, st), "router logits");
   }
   MOE_CUDA(moe::launch_router_topk(*L, L->logits, parts, bias, bstride, T, ids, w, st), "router top-k");
@@ -172,8 +172,9 @@ moe_status forward_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const
     return MOE_OK;
   }
   // (the gather below also clears the fp32 output accumulator)
-  MOE_CUDA(moe::launch_route_plan(*L, ids, w, T, st), "route plan");
-  if (moe::gemv_mma_supported(*L, T)) {
+  const bool gemv = moe::gemv_mma_supported(*L, T);
+  MOE_CUDA(moe::launch_route_plan(*L, ids, w, T, st, !gemv), "route plan");
+  if (gemv) {
     MOE_CUDA(moe::launch_gather_x16(*L, x, xdt, T, st), "gather");
     MOE_CUDA(moe::launch_gemv_mma(*L, st, ev ? ev + 1 : nullptr), "batched decode expert GEMVs");
   } else {
@@ -272,7 +273,7 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   const int64_t dn_total = (int64_t)(E + S) * L->dn_expert_bytes;
   ALLOC(L->gu, gu_total);
   ALLOC(L->dn, dn_total);
-  ALLOC(L->logits, sizeof(float) * (int64_t)moe::kRouterMaxParts * sh->max_tokens * E);
+  ALLOC(L->logits, sizeof(float) * moe::router_logits_floats(sh->max_tokens, E));
   ALLOC(L->offsets, sizeof(int) * (E + S + 1));
   ALLOC(L->active, sizeof(int) * (E + S + 1));
   ALLOC(L->route_token, sizeof(int) * (int64_t)L->max_routes);

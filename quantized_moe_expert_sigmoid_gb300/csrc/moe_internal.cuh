@@ -165,7 +165,19 @@ cudaError_t launch_repack(const uint8_t *src, int rows, int K, uint8_t *dst,
 // Large batches split H into parts whose partial logits are summed by the
 // top-k kernel in part order; `logits` holds parts * T * E floats.
 constexpr int kRouterMaxParts = 8;
-int router_parts(int T, int max_parts);
+// Batches of up to kRouterSmallT tokens have too few 32 x 64 tiles to fill
+// the GPU, so they split H into up to kRouterMaxPartsSmall parts instead.
+constexpr int kRouterSmallT = 128;
+constexpr int kRouterMaxPartsSmall = 32;
+// Logits floats a layer of max_tokens needs for the K-split parts.
+inline int64_t router_logits_floats(int max_tokens, int E) {
+  const int64_t a = (int64_t)kRouterMaxParts * max_tokens;
+  const int64_t b = (int64_t)kRouterMaxPartsSmall * (max_tokens < kRouterSmallT ? max_tokens : kRouterSmallT);
+  return (a > b ? a : b) * E;
+}
+// K parts for T tokens: 1 for T <= 16 (the one-pass kernel), else enough to
+// fill `sms` SMs (at most max_parts, and the small-batch or large-batch cap).
+int router_parts(int T, int E, int H, int sms, int max_parts);
 cudaError_t launch_router_logits(const Layer &L, const void *x, moe_dtype xdt, int T,
                                  const float *wr, float *logits, int parts, cudaStream_t stream);
 // sums the parts, adds the optional bias, selects; ids/weights [T][k]
@@ -174,8 +186,9 @@ cudaError_t launch_router_topk(const Layer &L, const float *logits, int parts, c
                                cudaStream_t stream);
 
 // plan.cu: histogram, prefix sum and stable permutation of the routes.
+// tiles: also write the tile lists of the tensor-core path.
 cudaError_t launch_route_plan(const Layer &L, const int32_t *ids, const float *weights,
-                              int T, cudaStream_t stream);
+                              int T, cudaStream_t stream, bool tiles);
 
 // combine.cu: the output of the batched path.  finalize: out = round(out_acc);
 // ordered: out[t] = sum over slots j in order of ybuf[route_pos[t*k+j]], then

@@ -210,10 +210,10 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(
 }  // namespace
 
 cudaError_t launch_route_plan(const Layer &L, const int32_t *ids, const float *weights, int T,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, bool tiles) {
   return count_and_check(launch_pdl(route_plan_kernel, dim3(1), dim3(1024), 0, stream, ids, weights, T, L.k,
                                     L.E, L.S, L.offsets, L.active, L.route_token, L.route_weight, L.err,
-                                    L.tiles_ug, L.tiles_dn, L.tile_counts, L.Fp / 128, L.Hp / 256,
+                                    tiles ? L.tiles_ug : nullptr, L.tiles_dn, L.tile_counts, L.Fp / 128, L.Hp / 256,
                                     tc_max_tiles(L, true), tc_max_tiles(L, false),
                                     L.deterministic ? L.route_pos : nullptr, tc_tile_routes(T)));
 }

@@ -209,14 +209,16 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
     if (e < E) {
       // the K-split parts, added in part order; unrolled so that their
       // loads are in flight together
-      float pz[kRouterMaxParts];
+      l = 0.f;
+      for (int z0 = 0; z0 < parts; z0 += kRouterMaxParts) {
+        float pz[kRouterMaxParts];
 #pragma unroll
-      for (int z = 0; z < kRouterMaxParts; ++z)
-        pz[z] = z < parts ? logits[(int64_t)z * T * E + (int64_t)t * E + e] : 0.f;
-      l = pz[0];
+        for (int z = 0; z < kRouterMaxParts; ++z)
+          pz[z] = z0 + z < parts ? logits[(int64_t)(z0 + z) * T * E + (int64_t)t * E + e] : 0.f;
 #pragma unroll
-      for (int z = 1; z < kRouterMaxParts; ++z)
-        if (z < parts) l += pz[z];
+        for (int z = 0; z < kRouterMaxParts; ++z)
+          if (z0 + z < parts) l = (z0 + z == 0) ? pz[z] : l + pz[z];
+      }
       const float b = bias ? bias[(int64_t)t * bstride + e] : 0.f;
       if (sel) {
         key = 1.0f / (1.0f + expf(-l)) + b;
@@ -273,8 +275,13 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
 
 }  // namespace
 
-int router_parts(int T, int max_parts) {
-  return T <= 16 ? 1 : std::max(1, std::min(max_parts, kRouterMaxParts));
+int router_parts(int T, int E, int H, int sms, int max_parts) {
+  if (T <= 16) return 1;
+  const int cap = T <= kRouterSmallT ? kRouterMaxPartsSmall : kRouterMaxParts;
+  const int tiles = ((T + kTM - 1) / kTM) * ((E + kTN - 1) / kTN);
+  const int nkc = (H + kKC - 1) / kKC;  // 32-wide K chunks
+  const int want = std::max(kRouterMaxParts, std::max(1, sms) / tiles);
+  return std::max(1, std::min(std::min(want, cap), std::min(max_parts, nkc)));
 }
 
 cudaError_t launch_router_logits(const Layer &L, const void *x, moe_dtype xdt, int T,
@@ -432,7 +439,11 @@ extern "C" moe_status moe_route_noalloc(const void *x, moe_dtype x_dtype, int32_
   L.scale = routed_scaling;
   L.sel_bias = 0;  // logit_bias is added to the logits
   cudaStream_t st = (cudaStream_t)stream;
-  const int parts = moe::router_parts(T, (int)(moe::kNoAllocMaxLogits / ((int64_t)T * n_experts)));
+  int dev = 0, sms = 1;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return report_error(MOE_ERR_CUDA, "moe_route_noalloc: device query failed");
+  const int parts = moe::router_parts(T, n_experts, hidden, sms,
+                                      (int)(moe::kNoAllocMaxLogits / ((int64_t)T * n_experts)));
   e = moe::launch_router_logits(L, x, x_dtype, T, router_w, logits, parts, st);
   if (e == cudaSuccess)
     e = moe::launch_router_topk(L, logits, parts, logit_bias, bias_row_stride, T, ids, weights, st);
