@@ -86,7 +86,8 @@ void free_layer(Layer *L) {
   void *ptrs[] = {L->gu, L->dn, L->logits, L->offsets, L->active, L->route_token,
                   L->route_weight, L->h32, L->out_acc, L->err, L->sync, L->x16, L->h16,
                   L->tiles_ug, L->tiles_dn, L->tile_counts, L->ybuf, L->route_pos,
-                  L->dense_ids, L->dense_w, L->rlog, L->x_stage, L->out_stage};
+                  L->dense_ids, L->dense_w, L->rlog, L->x_stage, L->out_stage, L->hr,
+                  L->hsh, L->useq, L->ulog};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   if (L->tev) {
@@ -279,6 +280,12 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   ALLOC(L->route_token, sizeof(int) * (int64_t)L->max_routes);
   ALLOC(L->route_weight, sizeof(float) * (int64_t)L->max_routes);
   ALLOC(L->h32, sizeof(float) * (int64_t)std::min(sh->max_tokens, moe::kFusedMaxTokens) * (k + S) * L->Fp);
+  if (L->unit_resident) {
+    ALLOC(L->hr, sizeof(float) * (int64_t)k * L->Fp);
+    ALLOC(L->hsh, sizeof(float) * (int64_t)L->Fp);
+    ALLOC(L->useq, sizeof(unsigned long long) * moe::unit_decode_seq_words());
+    ALLOC(L->ulog, sizeof(unsigned long long) * (int64_t)L->sms * E);
+  }
   ALLOC(L->out_acc, sizeof(float) * (int64_t)sh->max_tokens * H);
   ALLOC(L->err, sizeof(unsigned));
   ALLOC(L->sync, 4 * sizeof(unsigned));
@@ -313,6 +320,10 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
     if (e == cudaSuccess) e = moe::launch_fill(L->dense_w, 1.0f, sh->max_tokens, st);
   }
   if (e == cudaSuccess) e = cudaMemsetAsync(L->sync, 0, 4 * sizeof(unsigned), st);
+  if (e == cudaSuccess && L->useq)
+    e = cudaMemsetAsync(L->useq, 0, sizeof(unsigned long long) * moe::unit_decode_seq_words(), st);
+  if (e == cudaSuccess && L->ulog)
+    e = cudaMemsetAsync(L->ulog, 0, sizeof(unsigned long long) * (size_t)L->sms * E, st);
   if (e == cudaSuccess)
     e = cudaMemsetAsync(L->rlog, 0,
                         sizeof(unsigned long long) * moe::kLogitCopies * moe::kFusedMaxTokens * E, st);

@@ -1056,7 +1056,7 @@ cudaError_t decode_prepare(Layer &L) {
   if (e == cudaSuccess) e = prepare_tt<8, 0, 0>(&n[7]);
   if (e != cudaSuccess) return e;
   L.fused_resident = *std::min_element(n, n + 8) >= 1 ? 1 : 0;
-  return cudaSuccess;
+  return unit_decode_prepare(L);
 }
 
 bool fused_decode_supported(const Layer &L, int T) {
@@ -1070,6 +1070,8 @@ cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, in
                                 float *w_out, void *out, moe_dtype odt, cudaStream_t stream) {
   FusedPlan fp;
   if (!plan_fused(L, T, fp)) return cudaErrorInvalidConfiguration;
+  if (T == 1 && unit_decode_supported(L))
+    return launch_decode_unit(L, x, xdt, wr, bias, ids_in, w_in, ids_out, w_out, out, odt, stream);
   Params p;
   p.L = L;
   p.x = x;

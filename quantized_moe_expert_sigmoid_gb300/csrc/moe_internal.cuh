@@ -58,6 +58,8 @@ struct Layer {
   // the single-launch decode kernel's grid (one CTA per SM) can be resident
   // all at once: checked at create from the occupancy of every instance
   int fused_resident = 0;
+  // the one-token unit kernel's grid can be resident all at once (create)
+  int unit_resident = 0;
   // shape
   int H, E, k, F, S;  // S = number of shared experts (0 or 1)
   float scale;
@@ -83,6 +85,11 @@ struct Layer {
   int *route_token = nullptr;   // [max_routes]
   float *route_weight = nullptr; // [max_routes]
   float *h32 = nullptr;      // [min(max_tokens, 8) * (k+S)][Fp] SwiGLU output of the decode kernel
+  // one-token unit kernel (decode_unit.cu)
+  float *hr = nullptr;       // [k][Fp] the selected experts' SwiGLU outputs
+  float *hsh = nullptr;      // [Fp] the shared expert's SwiGLU output
+  unsigned long long *useq = nullptr;  // arrival counters (exit, shared h, h of each slot), never reset
+  unsigned long long *ulog = nullptr;  // [sms][E] tagged router logits, one private copy per CTA
   float *out_acc = nullptr;  // [max_tokens][H] fp32 accumulator
   // deterministic combine only (else nullptr)
   float *ybuf = nullptr;     // [max_routes][Hp] weighted down outputs, route order
@@ -207,6 +214,16 @@ size_t smem_limit_fused();
 // the current device (create)
 cudaError_t decode_prepare(Layer &L);
 bool fused_decode_supported(const Layer &L, int T);
+
+// decode_unit.cu: the whole layer for one token, split into (expert,
+// 32-output block) units; taken by launch_decode_fused at T = 1 when the
+// layer's shape has an instance (H padded to 3,584 or 2,560).
+cudaError_t unit_decode_prepare(Layer &L);
+int unit_decode_seq_words();
+bool unit_decode_supported(const Layer &L);
+cudaError_t launch_decode_unit(const Layer &L, const void *x, moe_dtype xdt, const float *wr, const float *bias,
+                               const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
+                               void *out, moe_dtype odt, cudaStream_t stream);
 cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, int T,
                                 const float *wr, const float *bias, int64_t bstride,
                                 const int32_t *ids_in, const float *w_in, int32_t *ids_out,
