@@ -9,7 +9,9 @@
 // HelloSun model card's whole-layer check: out = sum over the selected
 // experts of w * down(silu(gate x) * up x) + the shared expert):
 //   1. router logit of expert e on CTA G - E + e, published as a tagged word
-//      into every CTA's private copy; every CTA selects the top-k itself;
+//      into every CTA's private copy (copy c of logit e at [e][c]: a router's
+//      G stores are coalesced and no line has several writers); every CTA
+//      selects the top-k itself;
 //   2. the shared expert needs no routing, so its gate/up outputs are
 //      computed while the logits travel: CTA c takes outputs
 //      [c F / G, (c+1) F / G), four warps per output;
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
     float v = uwarp_sum(red[lane]);
     if (p.bias && !L.sel_bias) v += p.bias[my_e];
     if (tid < G)
-      st_relaxed_u64(&L.ulog[(int64_t)tid * E + my_e], ((unsigned long long)tag << 32) | __float_as_uint(v));
+      st_relaxed_u64(&L.ulog[(int64_t)my_e * G + tid], ((unsigned long long)tag << 32) | __float_as_uint(v));
   }
 
   // ---- while the logits travel: the top-k warp selects the experts and
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
       constexpr int kNl = NL;
       float lraw[kNl];
       bool have = false;
-      const unsigned long long *cp = L.ulog + (int64_t)c * E;
+      const unsigned long long *cp = L.ulog + c;  // this CTA's copy: logit e at cp[e * G]
       for (uint32_t poll = 0; poll < kUSpin && !have; ++poll) {
         bool mine = true;
 #pragma unroll
@@ -316,7 +318,7 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
           const int e = lane + 32 * i;
           lraw[i] = -FLT_MAX;
           if (e < E) {
-            const unsigned long long w = ld_relaxed_u64(cp + e);
+            const unsigned long long w = ld_relaxed_u64(cp + (int64_t)e * G);
             mine &= (uint32_t)(w >> 32) == tag;
             lraw[i] = __uint_as_float((uint32_t)w);
           }

@@ -89,7 +89,7 @@ struct Layer {
   float *hr = nullptr;       // [k][Fp] the selected experts' SwiGLU outputs
   float *hsh = nullptr;      // [Fp] the shared expert's SwiGLU output
   unsigned long long *useq = nullptr;  // arrival counters (exit, shared h, h of each slot), never reset
-  unsigned long long *ulog = nullptr;  // [sms][E] tagged router logits, one private copy per CTA
+  unsigned long long *ulog = nullptr;  // [E][sms] tagged router logits, one private copy per CTA
   float *out_acc = nullptr;  // [max_tokens][H] fp32 accumulator
   // deterministic combine only (else nullptr)
   float *ybuf = nullptr;     // [max_routes][Hp] weighted down outputs, route order
