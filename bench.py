@@ -77,7 +77,7 @@ METRIC = "MoE-layer tokens/s (expert-weight HBM GB/s as fraction of GB300 peak)"
 # from the ncu captures summarised in profiles/ (None when the kernel changed
 # after its capture).
 NCU_TRAFFIC = {
-    "decode1": 31_969_536,        # decode_fused_kernel<1,7,64>, ncu dram read + write per launch
+    "decode1": 32_045_568,        # decode_unit_kernel<14,2>, ncu dram read + write per launch
     "prefill4096": 457_219_328,   # grouped_gemm_tc<up/gate>, ncu dram read + write per launch
 }
 
@@ -404,13 +404,20 @@ def measure_layer(args, name, steps, warmup, world, rank, local_rank, dev, cpu_s
     torch.cuda.empty_cache()
 
     achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
+    if wl.n_layers > 1:
+        kname = "whole trunk step (every layer's calls and the residual RMSNorm launches)"
+    elif T == 1:
+        kname = "decode_unit_kernel (the step's only launch)"
+    elif T <= 8:
+        kname = "decode_fused_kernel (the step's only launch)"
+    else:
+        kname = "whole layer call (all launches of one step)"
     roofline = {"bound": "hbm",
-                "kernel": ("decode_fused_kernel (the step's only launch)" if T <= 8
-                           else "whole layer call (all launches of one step)"),
+                "kernel": kname,
                 "achieved": achieved, "peak": pk["hbm"], "peak_source": pk["hbm_src"],
                 "unit": "GB/s", "frac": achieved / pk["hbm"],
                 "algorithmic_bytes_per_launch": alg_bytes,
-                "traffic": NCU_TRAFFIC.get(name) if T <= 8 else None}
+                "traffic": NCU_TRAFFIC.get(name) if T <= 8 and wl.n_layers == 1 else None}
     out = {"value": world * T * steps / (ms / 1e3), "unit": "tokens/s", "steps": steps,
            "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3, "config": cfg,
            "expert_weight_gbs": expert_bytes / (ms_per_step * 1e-3) / 1e9,

@@ -145,9 +145,10 @@ typedef struct {
  * memory (PocketLLM design record, section 5: refuse at load, not inside a
  * request).  The layer belongs to the device current at create; create also
  * raises the kernels' shared-memory limits on that device and checks that the
- * single-launch decode kernel's grid (one CTA per SM, with device-wide waits
- * inside) can be resident all at once -- if not, batches of up to 8 tokens
- * run on the tensor-core kernels instead.  Runs on `stream` and synchronises
+ * single-launch decode kernels' grids (one CTA per SM, with device-wide waits
+ * inside: the one-token kernel for T = 1 on the Xing4 and K2-Horizon hidden
+ * sizes, the multi-token kernel for up to 8 tokens) can be resident all at
+ * once -- if not, those batches run on the other kernels instead.  Runs on `stream` and synchronises
  * it before returning, so the caller may free its weight buffers afterwards.
  * On success *out holds the layer; on failure *out is NULL and nothing is
  * leaked. */
@@ -192,9 +193,10 @@ moe_status moe_route(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_
  * The per-expert histogram, prefix sum and permutation run on the device
  * (PocketLLM design record, section 4: a CSR route table consumed by one
  * grouped kernel; section 6: the counts are never read back), so the call
- * is graph-capturable.  The single-launch decode kernel (T <= 8) holds every
- * SM of the device for the duration of the call and waits device-wide
- * inside, so it is launched as a cooperative launch: the runtime starts it
+ * is graph-capturable.  The single-launch decode kernels (T <= 8; T = 1 has
+ * its own, which splits the routed experts into 32-output units, one per SM)
+ * hold every SM of the device for the duration of the call and wait
+ * device-wide inside, so they are launched as cooperative launches: the runtime starts it
  * only once its whole grid can be resident, and refuses it (MOE_ERR_CUDA,
  * "too many blocks in cooperative launch") when the device cannot hold the
  * grid at all.  Its waits are bounded as well; one that gives up is reported
@@ -319,10 +321,11 @@ moe_status moe_layer_stage_times(moe_layer_t layer, float *ms, int32_t max_calls
 
 /* Test hook for the device-wait error path (no counterpart in the pages).
  *
- * moe_test_barrier_slack(layer, 1) makes the single-launch decode kernel
- * (batches of up to 8 tokens) expect one arrival more than its grid has at
- * its second grid-wide wait (every CTA's h written), so that the wait can
- * never be met: every CTA polls up to its bounded limit (2^21 reads of the
+ * moe_test_barrier_slack(layer, 1) makes the single-launch decode kernels
+ * (batches of up to 8 tokens) expect one arrival more than their grid can
+ * give at a device-wide wait (the multi-token kernel's wait for every CTA's
+ * h; the one-token kernel's wait for the first selected expert's h), so that
+ * the wait can never be met: every CTA polls up to its bounded limit (2^21 reads of the
  * counter, well under a minute), then finishes the call without the missing
  * arrival; moe_layer_check() returns MOE_ERR_TIMEOUT and the call's output
  * must not be used.  The layer stays usable: slack 0 restores normal calls.

@@ -129,7 +129,9 @@ __device__ __forceinline__ int dot_block32(const uint4 q, const uint4 h0, const 
   iq4_decode8(q.y, c2, c3);
   iq4_decode8(q.z, c4, c5);
   iq4_decode8(q.w, c6, c7);
-  return dot8_dp2a(c6, c7, h3, dot8_dp2a(c4, c5, h2, dot8_dp2a(c2, c3, h1, dot8_dp2a(c0, c1, h0, 0))));
+  // four independent chains of four dp2a (one chain of sixteen is
+  // latency-bound when few warps share the SM)
+  return (dot8_dp2a(c0, c1, h0, 0) + dot8_dp2a(c2, c3, h1, 0)) + (dot8_dp2a(c4, c5, h2, 0) + dot8_dp2a(c6, c7, h3, 0));
 }
 
 // Dynamic shared memory: ring (its start also holds the shared expert's
@@ -467,8 +469,10 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
       }
       L.hsh[fs0 + tid] = g / (1.0f + expf(-g)) * u;
     }
-    __syncthreads();
-    if (tid == 0) red_release_add64(&L.useq[kUSeqShared], 1ull);  // this CTA's shared h, ordered by the barrier
+    // (this CTA arrives on the shared counter after its routed units: a
+    // release waits until the CTA's earlier stores are acknowledged, which
+    // takes microseconds while the routed rows stream in, and thread 0
+    // computes a routed output)
   }
 
   // Quantised h of every expert, as the down projection reads it: block b
@@ -510,6 +514,8 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
     __syncthreads();
     if (tid == 0) red_release_add64(&L.useq[kUSeqSlot0 + slot], 1ull);
   }
+  __syncthreads();  // (the shared h stores above, for CTAs without a routed unit)
+  if (S && tid == 0) red_release_add64(&L.useq[kUSeqShared], 1ull);  // this CTA's shared h
 
   // ---- down projection of output rows [n0, n1), every expert in one pass,
   // once every counter is complete (thread j < k waits for slot j, thread k
@@ -557,20 +563,29 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
       }
     }
     __syncthreads();
+    // warp w: output row n0 + w.  Lane l takes block l (and l + 32, ...) of
+    // every selected expert's W_down row -- independent work the compiler
+    // interleaves -- summed in slot order per lane and then across the warp;
+    // the shared expert's row sum is added last.
     if (warp < nr) {
-      float out_v = 0.f;
-      for (int j = 0; j <= K; ++j) {  // slot order, then the shared expert
-        if (!((mask >> j) & 1u)) continue;
-        const uint8_t *row = dn_rows + (size_t)j * dn_slice + (size_t)warp * db;
-        float acc = 0.f;
-        for (int b = lane; b < NB; b += 32) {
-          const uint8_t *sb = row + (b >> 3) * kSBBytes;
-          const uint4 q = *reinterpret_cast<const uint4 *>(sb + 16 + (b & 7) * 16);
-          const float d = __half2float(*reinterpret_cast<const __half *>(sb + (b & 7) * 2));
-          const uint4 *hp = hq4 + (size_t)j * 4 * NB + b;
-          acc = fmaf((float)dot_block32(q, hp[0], hp[NB], hp[2 * NB], hp[3 * NB]), d * hs_q[j][b], acc);
-        }
-        out_v += uwarp_sum(acc);
+      auto block_dot = [&](int j, int b) -> float {
+        const uint8_t *sb = dn_rows + (size_t)j * dn_slice + (size_t)warp * db + (b >> 3) * kSBBytes;
+        const uint4 q = *reinterpret_cast<const uint4 *>(sb + 16 + (b & 7) * 16);
+        const float d = __half2float(*reinterpret_cast<const __half *>(sb + (b & 7) * 2));
+        const uint4 *hp = hq4 + (size_t)j * 4 * NB + b;
+        return (float)dot_block32(q, hp[0], hp[NB], hp[2 * NB], hp[3 * NB]) * (d * hs_q[j][b]);
+      };
+      float acc = 0.f;
+      for (int b = lane; b < NB; b += 32) {
+#pragma unroll
+        for (int j = 0; j < kUMaxK; ++j)
+          if (j < K && ((mask >> j) & 1u)) acc += block_dot(j, b);
+      }
+      float out_v = uwarp_sum(acc);
+      if (S) {
+        float sh = 0.f;
+        for (int b = lane; b < NB; b += 32) sh += block_dot(K, b);
+        out_v += uwarp_sum(sh);
       }
       if (lane == 0) {
         if (p.out_bf16)

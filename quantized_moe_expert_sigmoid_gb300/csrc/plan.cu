@@ -181,28 +181,39 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(
   }
 
   // tile lists of the tensor-core path: per active expert, route tiles of
-  // <= 256 and per route tile every weight tile, in the active order
+  // <= tile_routes and per route tile every weight tile, in the active
+  // order.  Entry (route tile rt, weight tile m) goes to rt * mtiles + m;
+  // every thread takes entries of both lists (a binary search over the
+  // active experts' first route tiles finds rt's expert), so no thread
+  // writes more than a few of them.
   if (ug) {
-    const int n_act = n_act_s;
-    for (int i = tid; i < n_act; i += blockDim.x) {
-      const int e = act[i];
+    const int n_act = n_act_s, nrt = n_rt_s;
+    if (tid == 0) tile_base[n_act] = nrt;
+    __syncthreads();
+    const int n_ug = nrt * ug_mtiles, n_all = n_ug + nrt * dn_mtiles;
+    for (int idx = tid; idx < n_all; idx += blockDim.x) {
+      const bool is_ug = idx < n_ug;
+      const int k = is_ug ? idx : idx - n_ug;
+      const int mt = is_ug ? ug_mtiles : dn_mtiles;
+      const int rt = k / mt, m = k - rt * mt;
+      int lo = 0, hi = n_act - 1;  // the last active expert whose first route tile is <= rt
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_base[mid] <= rt) lo = mid;
+        else hi = mid - 1;
+      }
+      const int e = act[lo], j = rt - tile_base[lo];
       const int beg = off[e], cntr = off[e + 1] - beg;
-      const int nrt = (cntr + tile_routes - 1) / tile_routes;
-      for (int j = 0; j < nrt; ++j) {
-        const int c = min(tile_routes, cntr - j * tile_routes);
-        for (int m = 0; m < ug_mtiles; ++m) {
-          const int idx = (tile_base[i] + j) * ug_mtiles + m;
-          if (idx < max_ug) ug[idx] = TcTile{e, m, beg + j * tile_routes, c};
-        }
-        for (int m = 0; m < dn_mtiles; ++m) {
-          const int idx = (tile_base[i] + j) * dn_mtiles + m;
-          if (idx < max_dn) dn[idx] = TcTile{e, m, beg + j * tile_routes, c};
-        }
+      const TcTile tt{e, m, beg + j * tile_routes, min(tile_routes, cntr - j * tile_routes)};
+      if (is_ug) {
+        if (k < max_ug) ug[k] = tt;
+      } else if (k < max_dn) {
+        dn[k] = tt;
       }
     }
     if (tid == 0) {
-      tile_counts[0] = min(n_rt_s * ug_mtiles, max_ug);
-      tile_counts[1] = min(n_rt_s * dn_mtiles, max_dn);
+      tile_counts[0] = min(nrt * ug_mtiles, max_ug);
+      tile_counts[1] = min(nrt * dn_mtiles, max_dn);
     }
   }
 }
