@@ -488,6 +488,7 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
   // ---- routed units: warp w computes output 32 b + w (both rows) and
   // SwiGLU; warp 0 quantises the unit's 32 h values (one block) and writes
   // them to global memory ----
+  int n_done = 0;  // units whose rows went through the ring before this one (a skipped unit issues none)
   for (int iu = 0; iu < n_mine; ++iu) {
     const int u = c + iu * G;
     const int slot = u / NB, b = u % NB;
@@ -499,7 +500,8 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
     float hv = 0.f;
     if (e >= 0) {
       const int s = warp / kUChunkOut;
-      if (!mbar_wait_ns(&full_bar[s], (uint32_t)iu & 1u, kUWaitNs)) atomicOr(&status, 2);
+      if (!mbar_wait_ns(&full_bar[s], (uint32_t)n_done & 1u, kUWaitNs)) atomicOr(&status, 2);
+      ++n_done;
       const uint8_t *rowg = ring + (size_t)s * kChunk + (warp % kUChunkOut) * kRB;
       float g, uu;
       upgate_part<NSB>(rowg, rowg + kUChunkOut * kRB, xq, sx, lane, 0, NSB / 2, g, uu);

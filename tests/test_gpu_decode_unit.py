@@ -1,0 +1,86 @@
+"""GPU parity of the one-token decode kernel (one launch per layer call at
+T = 1 on the Xing4 and K2-Horizon hidden sizes) on the paths the workload
+tests do not reach: caller-given routes with an invalid id and with one
+expert named in two slots, a plain logit bias (added before the sigmoid),
+and fp32 activations with a bf16 output -- each against the fp64 oracle.
+"""
+import functools
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+from oracle import cases
+from quantized_moe_expert_sigmoid_gb300 import MoeError, MoeLayer, moe_launch_count, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@functools.lru_cache(maxsize=None)
+def _setup(name):
+    wl = synth.WORKLOADS[name]
+    ew = parity.weights(0, 0, wl.E, wl.H, wl.F, 1)
+    L = MoeLayer.from_weights(ew, k=wl.k, scale=wl.scale, max_tokens=8)
+    c = cases.make_case(wl, T=1, ew=ew, seed=3)
+    x = torch.from_numpy(c.x.view(np.int16)).cuda().view(torch.bfloat16)
+    wr = torch.from_numpy(c.wr).cuda()
+    return wl, ew, L, c, x, wr
+
+
+@pytest.mark.parametrize("name", ["decode1", "k2h_decode1"])
+def test_given_routes_with_a_bad_and_a_repeated_id(name):
+    """Slot 1 names an expert outside [0, E): that route is dropped and
+    reported; slot 2 repeats slot 0's expert with another weight, so the
+    expert's output counts twice (w0 + w2)."""
+    wl, ew, L, c, x, wr = _setup(name)
+    ids = c.ids.copy()
+    ids[0, 1] = wl.E
+    ids[0, 2] = ids[0, 0]
+    w = np.linspace(0.3, 0.9, wl.k, dtype=np.float32)[None, :]
+    before = moe_launch_count()
+    out = L.forward(x, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), out_dtype=torch.float32)
+    assert moe_launch_count() - before == 1  # the whole layer in one launch
+    with pytest.raises(MoeError) as e:
+        L.check()
+    assert e.value.name == "MOE_ERR_BAD_EXPERT_ID"
+    L.check()
+    keep_ids, keep_w = ids.copy(), w.astype(np.float64)
+    keep_ids[0, 1], keep_w[0, 1] = 0, 0.0
+    ref = oracle.moe_forward(c.x64, keep_ids, keep_w, ew)
+    parity.assert_close_fp32(out.cpu().numpy(), ref, f"{name} bad and repeated ids")
+
+
+@pytest.mark.parametrize("name", ["decode1", "k2h_decode1"])
+def test_logit_bias_moves_the_selection(name):
+    """A [E] logit bias (added before the sigmoid, so it moves both the
+    selection and the weights) on one expert that the plain router did not
+    pick: ids must follow the oracle's biased routing."""
+    wl, ew, L, c, x, wr = _setup(name)
+    row = np.zeros(wl.E, np.float32)
+    outside = [e for e in range(wl.E) if e not in set(c.ids[0].tolist())]
+    row[outside[0]] = 4.0
+    out, ids, w = L.forward_routed(x, wr, torch.from_numpy(row).cuda(), out_dtype=torch.float32)
+    L.check()
+    ref_ids, ref_w, logits = oracle.route(c.x64, c.wr, wl.k, wl.scale, row)
+    assert oracle.min_topk_gap(logits, wl.k)[0] >= 1e-4
+    assert outside[0] in ref_ids[0]
+    np.testing.assert_array_equal(ids.cpu().numpy(), ref_ids)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=0, atol=2e-6)
+    ref = oracle.moe_forward(c.x64, ref_ids, ref_w, ew)
+    parity.assert_close_fp32(out.cpu().numpy(), ref, f"{name} logit bias")
+
+
+def test_fp32_activations_and_bf16_output():
+    """The same token as fp32 (bf16 values exactly) routes identically; the
+    bf16 output is the fp32 result rounded once."""
+    wl, ew, L, c, x, wr = _setup("decode1")
+    x32 = torch.from_numpy(synth.bf16_bits_to_f32(c.x).reshape(1, wl.H)).cuda()
+    out, ids, w = L.forward_routed(x32, wr, out_dtype=torch.bfloat16)
+    L.check()
+    np.testing.assert_array_equal(ids.cpu().numpy(), c.ids)
+    np.testing.assert_allclose(w.cpu().numpy(), c.w, rtol=0, atol=2e-6)
+    ref = oracle.moe_forward(c.x64, c.ids, c.w, ew)
+    parity.assert_close_bf16(out.float().cpu().numpy(), ref, "fp32 x, bf16 out")
