@@ -256,6 +256,28 @@ moe_status moe_layer_forward_routed_host(moe_layer_t layer, const void *x_host, 
 moe_status moe_residual_rmsnorm(float *resid, const void *delta, moe_dtype delta_dtype,
                                 void *u, int32_t T, int32_t H, float eps, void *stream);
 
+/* One step of a stack of layers on the fp32 residual stream: the residual
+ * update and RMS normalisation above, then this layer routed and applied to
+ * the normalised input (PocketLLM design record, section 2 for the residual
+ * stream; the layer as for moe_layer_forward_routed):
+ *   resid_out[t] = resid_in[t] + delta[t]   (delta NULL: resid_in[t])
+ *   u_out[t]     = bf16( resid_out[t] / sqrt(mean_c(resid_out[t][c]^2) + eps) )
+ *   ids, weights, out = the layer on u_out, as moe_layer_forward_routed.
+ * resid_in, resid_out [T][H] fp32 (they must not overlap: resid_out is a
+ * separate buffer, a caller stacking layers alternates two); delta [T][H]
+ * bf16 or fp32 (the previous layer's out) or NULL; u_out [T][H] bf16.  Every
+ * pointer is a device pointer, 16-byte aligned.  For one token on a layer
+ * whose one-token kernel applies, the whole step is that kernel's single
+ * launch (it forms u itself, with the same arithmetic as
+ * moe_residual_rmsnorm, bit for bit); otherwise it is moe_residual_rmsnorm's
+ * launch followed by moe_layer_forward_routed's.  Errors as for those two
+ * calls; MOE_ERR_INVALID_ARG when resid_out overlaps resid_in or delta. */
+moe_status moe_layer_forward_routed_resid(moe_layer_t layer, const float *resid_in, const void *delta,
+                                          moe_dtype delta_dtype, float *resid_out, void *u_out, float eps,
+                                          int32_t T, const float *router_w, const float *logit_bias,
+                                          int64_t bias_row_stride, int32_t *ids, float *weights, void *out,
+                                          moe_dtype out_dtype, void *stream);
+
 /* Router for callers that cannot allocate device memory.  The paper has no
  * counterpart: this entry point exists for callers that may not call
  * cudaMalloc themselves or let a library do it -- code inside a host

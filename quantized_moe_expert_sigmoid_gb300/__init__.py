@@ -30,7 +30,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 EXPORTS = ["moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
            "moe_layer_forward_routed", "moe_residual_rmsnorm", "moe_layer_check",
            "moe_layer_weight_bytes", "moe_launch_count", "moe_status_string", "moe_last_error",
-           "moe_route_noalloc", "moe_dense_forward"]
+           "moe_route_noalloc", "moe_dense_forward", "moe_layer_forward_routed_resid"]
 
 
 class MoeError(RuntimeError):
@@ -78,6 +78,7 @@ def load_library(path: str | None = None):
     lib.moe_layer_forward_routed.argtypes = [P, P, I32, I32, P, P, I64, P, P, P, I32, P]
     lib.moe_layer_forward_routed_host.argtypes = [P, P, I32, I32, P, P, I64, P, P, P, I32, P]
     lib.moe_residual_rmsnorm.argtypes = [P, P, I32, P, I32, I32, F, P]
+    lib.moe_layer_forward_routed_resid.argtypes = [P, P, P, I32, P, P, F, I32, P, P, I64, P, P, P, I32, P]
     lib.moe_layer_check.argtypes = [P]
     lib.moe_layer_weight_bytes.argtypes = [P]
     lib.moe_layer_weight_bytes.restype = I64
@@ -95,7 +96,7 @@ def load_library(path: str | None = None):
     for n in ("moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
               "moe_layer_forward_routed", "moe_residual_rmsnorm", "moe_layer_check",
               "moe_layer_enable_timing", "moe_layer_stage_times", "moe_dense_forward",
-              "moe_test_barrier_slack", "moe_layer_forward_routed_host"):
+              "moe_test_barrier_slack", "moe_layer_forward_routed_host", "moe_layer_forward_routed_resid"):
         getattr(lib, n).restype = I32
     _lib = lib
     return lib
@@ -208,6 +209,20 @@ def moe_layer_forward_routed(layer, x, router_w, ids, weights, out, logit_bias=N
     _check(load_library().moe_layer_forward_routed(
         ctypes.c_void_p(layer), _ptr(x, "x", d["x"]), _dtype(x), x.shape[0],
         _ptr(router_w, "router_w", d["f32"]), bias_p, bias_row_stride,
+        _ptr(ids, "ids", d["i32"]), _ptr(weights, "weights", d["f32"]), _ptr(out, "out", d["x"]),
+        _dtype(out), _stream(stream)))
+
+
+def moe_layer_forward_routed_resid(layer, resid_in, delta, resid_out, u_out, eps, router_w, ids, weights, out,
+                                   logit_bias=None, stream=None):
+    T = resid_in.shape[0]
+    d = _dt()
+    ddt = MOE_DT_FP32 if delta is None else _dtype(delta)
+    bias_stride = 0 if logit_bias is None or logit_bias.dim() == 1 else logit_bias.stride(0)
+    _check(load_library().moe_layer_forward_routed_resid(
+        ctypes.c_void_p(layer), _ptr(resid_in, "resid_in", d["f32"]), _ptr(delta, "delta", d["x"]), ddt,
+        _ptr(resid_out, "resid_out", d["f32"]), _ptr(u_out, "u_out", (d["x"][0],)), float(eps), T,
+        _ptr(router_w, "router_w", d["f32"]), _ptr(logit_bias, "logit_bias", d["f32"]), bias_stride,
         _ptr(ids, "ids", d["i32"]), _ptr(weights, "weights", d["f32"]), _ptr(out, "out", d["x"]),
         _dtype(out), _stream(stream)))
 
@@ -402,10 +417,12 @@ class MoeTrunk:
     """A stack of MoE layers on an fp32 residual stream (the 38-layer trunk
     of the Xing4.0-29B-A4B model card, MoE blocks only):
         r_0 = x,  u_l = bf16(r_l / sqrt(mean(r_l^2) + eps)),  r_{l+1} = r_l + MoE_l(u_l).
-    Per layer: one residual-add + RMSNorm launch, then the layer's
-    route + forward launches (layer outputs are fp32, added to r in fp32).
-    Every tensor it uses is preallocated at construction, so forward() can
-    be captured in a CUDA graph."""
+    Per layer one moe_layer_forward_routed_resid call: the residual update,
+    the RMSNorm and the layer (at one token a single launch of the one-token
+    kernel; otherwise a residual-RMSNorm launch and the layer's launches).
+    The residual alternates between two buffers (a step reads one and writes
+    the other); layer outputs are fp32.  Every tensor it uses is preallocated
+    at construction, so forward() can be captured in a CUDA graph."""
 
     def __init__(self, layers, routers, max_tokens, eps=1e-6, device="cuda"):
         import torch
@@ -413,7 +430,7 @@ class MoeTrunk:
         self.layers, self.routers, self.eps = list(layers), list(routers), float(eps)
         H, k = layers[0].H, layers[0].k
         n = len(layers)
-        self.r = torch.empty((max_tokens, H), dtype=torch.float32, device=device)
+        self.rbuf = [torch.empty((max_tokens, H), dtype=torch.float32, device=device) for _ in range(2)]
         self.u = [torch.empty((max_tokens, H), dtype=torch.bfloat16, device=device) for _ in range(n)]
         self.out = [torch.empty((max_tokens, H), dtype=torch.float32, device=device) for _ in range(n)]
         self.ids = [torch.empty((max_tokens, k), dtype=torch.int32, device=device) for _ in range(n)]
@@ -422,18 +439,20 @@ class MoeTrunk:
 
     def forward(self, x, stream=None):
         """x: fp32 or bf16 [T, H] on the device.  Returns the final residual
-        r_L [T, H] fp32 (a view of the trunk's buffer); the per-layer u, out,
-        ids and w stay readable in self.u / self.out / self.ids / self.w."""
+        r_L [T, H] fp32 (a view of one of the trunk's buffers); the per-layer
+        u, out, ids and w stay readable in self.u / self.out / self.ids /
+        self.w."""
         T = x.shape[0]
-        r = self.r[:T]
-        r.copy_(x)
+        cur = 0
+        self.rbuf[0][:T].copy_(x)
         prev = None
         for l, (L, wr) in enumerate(zip(self.layers, self.routers)):
-            u = self.u[l][:T]
-            moe_residual_rmsnorm(r, prev, u, self.eps, stream=stream)
-            out = self.out[l][:T]
-            moe_layer_forward_routed(L.handle, u, wr, self.ids[l][:T], self.w[l][:T], out, stream=stream)
-            prev = out
+            r_in, r_out = self.rbuf[cur][:T], self.rbuf[1 - cur][:T]
+            moe_layer_forward_routed_resid(L.handle, r_in, prev, r_out, self.u[l][:T], self.eps, wr,
+                                           self.ids[l][:T], self.w[l][:T], self.out[l][:T], stream=stream)
+            prev = self.out[l][:T]
+            cur = 1 - cur
+        r = self.rbuf[cur][:T]
         moe_residual_rmsnorm(r, prev, self.u_final[:T], self.eps, stream=stream)  # r_L = r_{L-1} + out
         return r
 

@@ -483,9 +483,56 @@ moe_status moe_residual_rmsnorm(float *resid, const void *delta, moe_dtype delta
   if (!resid || !u) return fail(MOE_ERR_INVALID_ARG, "resid and u must be non-NULL");
   if (!moe::aligned(resid, 16) || !moe::aligned(u, 16) || (delta && !moe::aligned(delta, 16)))
     return fail(MOE_ERR_MISALIGNED, "resid, delta and u must be 16-byte aligned");
-  MOE_CUDA(moe::launch_residual_rmsnorm(resid, delta, delta_dtype, u, T, H, eps, (cudaStream_t)stream),
+  MOE_CUDA(moe::launch_residual_rmsnorm(resid, delta, delta_dtype, resid, u, T, H, eps, (cudaStream_t)stream),
            "residual rmsnorm");
   return MOE_OK;
+}
+
+moe_status moe_layer_forward_routed_resid(moe_layer_t layer, const float *resid_in, const void *delta,
+                                          moe_dtype delta_dtype, float *resid_out, void *u_out, float eps,
+                                          int32_t T, const float *router_w, const float *logit_bias,
+                                          int64_t bias_row_stride, int32_t *ids, float *weights, void *out,
+                                          moe_dtype out_dtype, void *stream) {
+  Layer *L = reinterpret_cast<Layer *>(layer);
+  if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d is negative", T);
+  if (T > L->max_tokens) return fail(MOE_ERR_TOO_MANY_TOKENS, "T = %d exceeds max_tokens = %d", T, L->max_tokens);
+  if (delta_dtype != MOE_DT_BF16 && delta_dtype != MOE_DT_FP32)
+    return fail(MOE_ERR_INVALID_ARG, "delta_dtype %d is not MOE_DT_BF16 or MOE_DT_FP32", (int)delta_dtype);
+  if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
+  if (out_dtype != MOE_DT_BF16 && out_dtype != MOE_DT_FP32)
+    return fail(MOE_ERR_INVALID_ARG, "out_dtype %d is not MOE_DT_BF16 or MOE_DT_FP32", (int)out_dtype);
+  if (L->H % 8) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "hidden %d is not a multiple of 8", L->H);
+  if (T == 0) return MOE_OK;
+  if (!resid_in || !resid_out || !u_out || !out || !router_w || !ids || !weights)
+    return fail(MOE_ERR_INVALID_ARG, "resid_in, resid_out, u_out, out, router_w, ids and weights must be non-NULL");
+  const size_t rb = sizeof(float) * (size_t)T * L->H;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(resid_in), b0 = reinterpret_cast<uintptr_t>(resid_out);
+  if (a0 < b0 + rb && b0 < a0 + rb) return fail(MOE_ERR_INVALID_ARG, "resid_in and resid_out overlap");
+  if (delta) {
+    const size_t db = (delta_dtype == MOE_DT_BF16 ? 2 : 4) * (size_t)T * L->H;
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(delta);
+    if (d0 < b0 + rb && b0 < d0 + db) return fail(MOE_ERR_INVALID_ARG, "delta and resid_out overlap");
+  }
+  if (!moe::aligned(resid_in, 16) || !moe::aligned(resid_out, 16) || !moe::aligned(u_out, 16) ||
+      (delta && !moe::aligned(delta, 16)) || !moe::aligned(out, 16) || !moe::aligned(router_w, 16))
+    return fail(MOE_ERR_MISALIGNED, "resid_in, delta, resid_out, u_out, out and router_w must be 16-byte aligned");
+  if (!moe::aligned(ids, 4) || !moe::aligned(weights, 4))
+    return fail(MOE_ERR_MISALIGNED, "ids/weights are not 4-byte aligned");
+  if (logit_bias && bias_row_stride < 0) return fail(MOE_ERR_INVALID_ARG, "bias_row_stride is negative");
+  cudaStream_t st = (cudaStream_t)stream;
+  if (T == 1 && moe::unit_decode_supported(*L)) {
+    const moe::ResidStep rs{resid_in, delta, delta_dtype == MOE_DT_BF16 ? 1 : 0, resid_out,
+                            reinterpret_cast<__nv_bfloat16 *>(u_out), eps};
+    MOE_CUDA(moe::launch_decode_unit(*L, u_out, MOE_DT_BF16, router_w, logit_bias, nullptr, nullptr, ids, weights,
+                                     out, out_dtype, st, &rs),
+             "one-token decode");
+    return MOE_OK;
+  }
+  MOE_CUDA(moe::launch_residual_rmsnorm(resid_in, delta, delta_dtype, resid_out, u_out, T, L->H, eps, st),
+           "residual rmsnorm");
+  return moe_layer_forward_routed(layer, u_out, MOE_DT_BF16, T, router_w, logit_bias, bias_row_stride, ids,
+                                  weights, out, out_dtype, stream);
 }
 
 moe_status moe_layer_enable_timing(moe_layer_t layer, int32_t calls) {

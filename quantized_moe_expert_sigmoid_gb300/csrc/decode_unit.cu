@@ -62,6 +62,7 @@ constexpr int kUShStage = kUStages - 2;  // the shared gate/up rows wait in ring
 constexpr int kUMaxRows = 32;           // output rows per CTA (one warp each)
 constexpr int kUMaxNB = 32;             // F <= 1024: 32-blocks of h per expert
 constexpr int kUTopkWarp = kUW - 1;     // selects the experts while the others compute
+constexpr int kUMaxH = 4096;            // a residual-stream step: 256 threads x 8 elements x 2
 constexpr uint32_t kUSpin = 1u << 21;   // counter polls before giving up (each an L2 round trip)
 constexpr uint64_t kUWaitNs = 500000000ull;
 
@@ -81,6 +82,7 @@ struct UParams {
   void *out;
   int out_bf16;
   int wr_smem;  // 1: the router row is bulk-copied into shared memory
+  ResidStep rs;  // rs.r_in != nullptr: x is formed from the residual stream here
   int nr_max;   // largest output-row slice of a CTA (sizes the W_down row region)
 };
 
@@ -193,6 +195,8 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
   __shared__ float sel_w[kUMaxK];
   __shared__ float red[kUW], part_g[kUW], part_u[kUW];
   __shared__ float hs_q[kUMaxK + 1][kUMaxNB];
+  __shared__ __align__(16) uint16_t xs_s[kUMaxH];  // x formed from the residual stream (bf16)
+  __shared__ float red8[8];
 
   const Layer &L = p.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -270,6 +274,79 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
   pdl_launch_dependents();
   pdl_wait();  // x, the outputs and the counters may belong to the previous grid
 
+  // ---- a trunk step: r_out = r_in + delta and x = u = bf16(rmsnorm(r_out)),
+  // computed by every CTA for the whole token (3,584 values) with the
+  // arithmetic of the separate residual-RMSNorm kernel (threads 0..255, 8
+  // elements each per 2,048, the 8 warp sums added in order), so u is the
+  // same bit for bit; CTA 0 also writes r_out and u ----
+  const void *xsrc = p.x;
+  int xbf = p.x_bf16;
+  if (p.rs.r_in) {
+    float v[2][8];
+    if (warp < 8) {
+      float ss = 0.f;
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const int cc = tid * 8 + 2048 * m;
+        if (cc < H) {
+          const float4 a = *reinterpret_cast<const float4 *>(p.rs.r_in + cc);
+          const float4 b2 = *reinterpret_cast<const float4 *>(p.rs.r_in + cc + 4);
+          v[m][0] = a.x; v[m][1] = a.y; v[m][2] = a.z; v[m][3] = a.w;
+          v[m][4] = b2.x; v[m][5] = b2.y; v[m][6] = b2.z; v[m][7] = b2.w;
+          if (p.rs.delta) {
+            if (p.rs.delta_bf16) {
+              const uint4 d = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.rs.delta) + cc);
+              const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                v[m][2 * i] += __uint_as_float(dw[i] << 16);
+                v[m][2 * i + 1] += __uint_as_float(dw[i] & 0xFFFF0000u);
+              }
+            } else {
+              const float4 d0 = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.rs.delta) + cc);
+              const float4 d1 = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.rs.delta) + cc + 4);
+              v[m][0] += d0.x; v[m][1] += d0.y; v[m][2] += d0.z; v[m][3] += d0.w;
+              v[m][4] += d1.x; v[m][5] += d1.y; v[m][6] += d1.z; v[m][7] += d1.w;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ss = fmaf(v[m][i], v[m][i], ss);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) red8[warp] = ss;
+    }
+    __syncthreads();
+    if (warp < 8) {
+      float tot = 0.f;
+      for (int i = 0; i < 8; ++i) tot += red8[i];
+      const float inv = 1.0f / sqrtf(tot / (float)H + p.rs.eps);
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const int cc = tid * 8 + 2048 * m;
+        if (cc < H) {
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 bb = __floats2bfloat162_rn(v[m][2 * i] * inv, v[m][2 * i + 1] * inv);
+            o[i] = *reinterpret_cast<uint32_t *>(&bb);
+          }
+          const uint4 packed = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4 *>(xs_s + cc) = packed;
+          if (c == 0) {
+            *reinterpret_cast<float4 *>(p.rs.r_out + cc) = make_float4(v[m][0], v[m][1], v[m][2], v[m][3]);
+            *reinterpret_cast<float4 *>(p.rs.r_out + cc + 4) = make_float4(v[m][4], v[m][5], v[m][6], v[m][7]);
+            *reinterpret_cast<uint4 *>(p.rs.u_out + cc) = packed;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    xsrc = xs_s;
+    xbf = 1;
+  }
+
   if (tid == 0) {
     epoch_s = ld_acquire64(&L.useq[kUSeqExit]) / (unsigned long long)G;
     if (S && nr > 0) {  // the shared expert's W_down rows of this CTA's output rows
@@ -286,8 +363,8 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
     const float *w = p.wr_smem ? wrs : p.wr + (int64_t)my_e * H;
     float acc = 0.f;
     for (int i = tid; i < H; i += kUT) {
-      const float xv = p.x_bf16 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(p.x)[i] << 16)
-                                : reinterpret_cast<const float *>(p.x)[i];
+      const float xv = xbf ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(xsrc)[i] << 16)
+                           : reinterpret_cast<const float *>(xsrc)[i];
       acc = fmaf(xv, w[i], acc);
     }
     acc = uwarp_sum(acc);
@@ -412,8 +489,8 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
     for (int j = tid; j < kHp / 8 && warp != kUTopkWarp; j += kUT) {
       const int e0 = j * 8;
       float v[8];
-      if (p.x_bf16 && e0 + 8 <= H) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.x) + e0);
+      if (xbf && e0 + 8 <= H) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(xsrc) + e0);
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
   #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -424,8 +501,8 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
   #pragma unroll
         for (int q = 0; q < 8; ++q)
           v[q] = e0 + q >= H ? 0.f
-                 : p.x_bf16 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(p.x)[e0 + q] << 16)
-                            : reinterpret_cast<const float *>(p.x)[e0 + q];
+                 : xbf ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(xsrc)[e0 + q] << 16)
+                       : reinterpret_cast<const float *>(xsrc)[e0 + q];
       }
       float m = 0.f;
   #pragma unroll
@@ -631,8 +708,19 @@ int unit_nl(const Layer &L) { return L.E <= 64 ? 2 : 4; }
 // device, not to one layer); the occupancy check uses this layer's size.
 template <int NSB, int NL>
 cudaError_t unit_prepare_one(const Layer &L, int *per_sm) {
-  cudaError_t e = cudaFuncSetAttribute(decode_unit_kernel<NSB, NL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem_limit_fused());
+  // the dynamic limit is what the device allows a block beyond the
+  // kernel's static shared memory
+  cudaFuncAttributes fa;
+  int optin = 0;
+  cudaError_t e = cudaFuncGetAttributes(&fa, decode_unit_kernel<NSB, NL>);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, L.device);
+  if (e != cudaSuccess) return e;
+  const size_t limit = optin > (int)fa.sharedSizeBytes ? (size_t)optin - fa.sharedSizeBytes : 0;
+  if (unit_smem<NSB>(L) > limit) {
+    *per_sm = 0;  // does not fit: this layer's one-token calls take the multi-token kernel
+    return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(decode_unit_kernel<NSB, NL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, decode_unit_kernel<NSB, NL>, kUT, unit_smem<NSB>(L));
 }
@@ -670,7 +758,7 @@ bool unit_shape_ok(const Layer &L) {
   if ((int64_t)NB * 64 > (int64_t)kUStages * 8 * nsb * kSBBytes) return false;  // quantised h fits the ring
   if ((int64_t)std::max(L.H, L.Fp) * G >= ((int64_t)1 << 32)) return false;   // 32-bit splits
   const size_t smem = nsb == 14 ? unit_smem<14>(L) : unit_smem<10>(L);
-  return smem <= smem_limit_fused();
+  return smem <= 232448;  // the exact bound (static + dynamic) is checked when the layer is prepared
 }
 
 }  // namespace
@@ -695,12 +783,14 @@ bool unit_decode_supported(const Layer &L) {
 
 cudaError_t launch_decode_unit(const Layer &L, const void *x, moe_dtype xdt, const float *wr, const float *bias,
                                const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
-                               void *out, moe_dtype odt, cudaStream_t stream) {
+                               void *out, moe_dtype odt, cudaStream_t stream, const ResidStep *rs) {
   if (!unit_decode_supported(L)) return cudaErrorInvalidConfiguration;
+  if (rs && (L.H > kUMaxH || L.H % 8)) return cudaErrorInvalidConfiguration;
   UParams p;
   p.L = L;
   p.x = x;
   p.x_bf16 = xdt == MOE_DT_BF16;
+  p.rs = rs ? *rs : ResidStep{nullptr, nullptr, 0, nullptr, nullptr, 0.f};
   p.wr = wr;
   p.bias = bias;
   p.ids_in = ids_in;

@@ -221,9 +221,20 @@ bool fused_decode_supported(const Layer &L, int T);
 cudaError_t unit_decode_prepare(Layer &L);
 int unit_decode_seq_words();
 bool unit_decode_supported(const Layer &L);
+// The layer input of one trunk step, formed inside the one-token kernel:
+// r_out = r_in + delta, u = bf16(rmsnorm(r_out)), x = u (CTA 0 writes r_out
+// and u; r_in and r_out must not overlap).
+struct ResidStep {
+  const float *r_in;
+  const void *delta;   // nullable
+  int delta_bf16;
+  float *r_out;
+  __nv_bfloat16 *u_out;
+  float eps;
+};
 cudaError_t launch_decode_unit(const Layer &L, const void *x, moe_dtype xdt, const float *wr, const float *bias,
                                const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
-                               void *out, moe_dtype odt, cudaStream_t stream);
+                               void *out, moe_dtype odt, cudaStream_t stream, const ResidStep *rs = nullptr);
 cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, int T,
                                 const float *wr, const float *bias, int64_t bstride,
                                 const int32_t *ids_in, const float *w_in, int32_t *ids_out,
@@ -262,7 +273,8 @@ cudaError_t launch_gemv_mma(const Layer &L, cudaStream_t stream, cudaEvent_t *ev
 cudaError_t launch_gather_x16(const Layer &L, const void *x, moe_dtype xdt, int T, cudaStream_t stream);
 
 // norm.cu
-cudaError_t launch_residual_rmsnorm(float *resid, const void *delta, moe_dtype ddt,
+// r_out = r_in + delta (delta may be NULL; r_out may be r_in), u = bf16(rmsnorm(r_out))
+cudaError_t launch_residual_rmsnorm(const float *resid_in, const void *delta, moe_dtype ddt, float *resid_out,
                                     void *u, int T, int H, float eps, cudaStream_t stream);
 
 }  // namespace moe

@@ -1,7 +1,8 @@
 // Residual update and unweighted RMS normalisation between stacked layers
 // (PocketLLM "Xing4.0-29B-A4B: the design record", section 2: the residual
 // streams are carried in fp32 while the sublayer is handed the narrow type).
-//   resid[t] += delta[t];  u[t] = bf16(resid[t] / sqrt(mean(resid[t]^2) + eps))
+//   r_out[t] = r_in[t] + delta[t];  u[t] = bf16(r_out[t] / sqrt(mean(r_out[t]^2) + eps))
+// (r_out may be r_in: the update in place)
 // One CTA per token, 8 elements per thread per step, fp32 throughout, one
 // round-to-nearest-even to bf16 at the end.
 #include "device_utils.cuh"
@@ -28,24 +29,28 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float v[8]) {
 }
 
 template <typename DT>
-__global__ void __launch_bounds__(256) residual_rmsnorm_kernel(float *__restrict__ resid,
-                                                               const DT *__restrict__ delta, int H,
-                                                               float eps,
+__global__ void __launch_bounds__(256) residual_rmsnorm_kernel(const float *resid_in,
+                                                               const DT *__restrict__ delta, float *resid_out,
+                                                               int H, float eps,
                                                                __nv_bfloat16 *__restrict__ u) {
   __shared__ float red[8];
   const int t = blockIdx.x;
   pdl_wait();  // the residual and the layer output come from earlier launches
   pdl_launch_dependents();
-  float *r = resid + (int64_t)t * H;
+  const float *ri = resid_in + (int64_t)t * H;
+  float *r = resid_out + (int64_t)t * H;
+  const bool write = delta != nullptr || resid_in != resid_out;
   float ss = 0.f;
   for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
     float v[8];
-    load8(r + c, v);
+    load8(ri + c, v);
     if (delta) {
       float d[8];
       load8(delta + (int64_t)t * H + c, d);
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] += d[i];
+    }
+    if (write) {
       reinterpret_cast<float4 *>(r + c)[0] = make_float4(v[0], v[1], v[2], v[3]);
       reinterpret_cast<float4 *>(r + c)[1] = make_float4(v[4], v[5], v[6], v[7]);
     }
@@ -74,14 +79,15 @@ __global__ void __launch_bounds__(256) residual_rmsnorm_kernel(float *__restrict
 
 }  // namespace
 
-cudaError_t launch_residual_rmsnorm(float *resid, const void *delta, moe_dtype ddt, void *u,
-                                    int T, int H, float eps, cudaStream_t stream) {
+cudaError_t launch_residual_rmsnorm(const float *resid_in, const void *delta, moe_dtype ddt, float *resid_out,
+                                    void *u, int T, int H, float eps, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   if (ddt == MOE_DT_BF16)
     return count_and_check(launch_pdl(residual_rmsnorm_kernel<__nv_bfloat16>, dim3(T), dim3(256), 0, stream,
-                                      resid, (const __nv_bfloat16 *)delta, H, eps, (__nv_bfloat16 *)u));
-  return count_and_check(launch_pdl(residual_rmsnorm_kernel<float>, dim3(T), dim3(256), 0, stream, resid,
-                                    (const float *)delta, H, eps, (__nv_bfloat16 *)u));
+                                      resid_in, (const __nv_bfloat16 *)delta, resid_out, H, eps,
+                                      (__nv_bfloat16 *)u));
+  return count_and_check(launch_pdl(residual_rmsnorm_kernel<float>, dim3(T), dim3(256), 0, stream, resid_in,
+                                    (const float *)delta, resid_out, H, eps, (__nv_bfloat16 *)u));
 }
 
 }  // namespace moe

@@ -92,6 +92,8 @@ def test_null_layer_rejected(lib):
     assert lib.moe_layer_forward_routed_host(None, None, 0, 1, None, None, 0, None, None, None, 0, None) == 1
     assert lib.moe_route(None, None, 0, 0, None, None, 0, None, None, None) == 1
     assert lib.moe_forward(None, None, 0, 0, None, None, None, 0, None) == 1
+    assert lib.moe_layer_forward_routed_resid(None, None, None, 1, None, None, 1e-6, 1, None, None, 0,
+                                              None, None, None, 0, None) == 1
     assert lib.moe_layer_destroy(None) == 0
     assert lib.moe_layer_weight_bytes(None) == -1
 

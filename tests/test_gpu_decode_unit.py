@@ -84,3 +84,71 @@ def test_fp32_activations_and_bf16_output():
     np.testing.assert_allclose(w.cpu().numpy(), c.w, rtol=0, atol=2e-6)
     ref = oracle.moe_forward(c.x64, c.ids, c.w, ew)
     parity.assert_close_bf16(out.float().cpu().numpy(), ref, "fp32 x, bf16 out")
+
+
+@pytest.mark.parametrize("name", ["decode1", "k2h_decode1"])
+@pytest.mark.parametrize("delta_kind", ["none", "bf16", "fp32"])
+def test_residual_step_in_the_one_token_launch(name, delta_kind):
+    """moe_layer_forward_routed_resid at one token forms the residual update
+    and the RMSNorm inside the one-token kernel's single launch.  Its r_out,
+    u, ids, weights and output must equal, bit for bit, the same step taken
+    as a residual-RMSNorm launch followed by moe_layer_forward_routed; and u
+    must be the bf16 RMSNorm of r_in + delta within one bf16 ulp of the
+    fp64 oracle."""
+    from quantized_moe_expert_sigmoid_gb300 import (moe_layer_forward_routed, moe_layer_forward_routed_resid,
+                                                    moe_residual_rmsnorm)
+    wl, ew, L, c, x, wr = _setup(name)
+    g = torch.Generator().manual_seed(11)
+    r_in = (torch.randn(1, wl.H, generator=g) * 0.7).cuda()
+    delta = None
+    if delta_kind != "none":
+        d = torch.randn(1, wl.H, generator=g) * 0.3
+        delta = (d.to(torch.bfloat16) if delta_kind == "bf16" else d).cuda()
+    eps = 1e-6
+
+    def bufs():
+        return (torch.full((1, wl.H), float("nan"), device="cuda"),
+                torch.zeros(1, wl.H, dtype=torch.bfloat16, device="cuda"),
+                torch.full((1, wl.k), -7, dtype=torch.int32, device="cuda"),
+                torch.zeros(1, wl.k, device="cuda"), torch.zeros(1, wl.H, device="cuda"))
+
+    r1, u1, i1, w1, o1 = bufs()
+    before = moe_launch_count()
+    moe_layer_forward_routed_resid(L.handle, r_in, delta, r1, u1, eps, wr, i1, w1, o1)
+    assert moe_launch_count() - before == 1  # residual, RMSNorm and the layer in one launch
+    L.check()
+    r2, u2, i2, w2, o2 = bufs()
+    r2.copy_(r_in)
+    moe_residual_rmsnorm(r2, delta, u2, eps)
+    moe_layer_forward_routed(L.handle, u2, wr, i2, w2, o2)
+    L.check()
+    for a, b, what in ((r1, r2, "r_out"), (u1.view(torch.int16), u2.view(torch.int16), "u"), (i1, i2, "ids"),
+                       (w1, w2, "weights"), (o1, o2, "out")):
+        assert torch.equal(a, b), f"{name} delta {delta_kind}: {what} differs from the two-launch step"
+    r_ref = r_in.cpu().numpy().astype(np.float32)
+    if delta is not None:
+        r_ref = (r_ref + delta.float().cpu().numpy()).astype(np.float32)
+    np.testing.assert_array_equal(r1.cpu().numpy(), r_ref)
+    u_ref = synth.to_bf16_bits(np.asarray(oracle.rmsnorm(r_ref.astype(np.float64), eps), np.float32))
+    u_bits = u1.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.abs(u_bits.astype(np.int32) - u_ref.astype(np.int32)).max() <= 1
+    # the input buffer is read only
+    assert torch.isfinite(r_in).all()
+
+
+def test_residual_step_rejects_overlap():
+    from quantized_moe_expert_sigmoid_gb300 import moe_layer_forward_routed_resid
+    wl, ew, L, c, x, wr = _setup("decode1")
+    r = torch.zeros(2, wl.H, device="cuda")
+    u = torch.zeros(1, wl.H, dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros(1, wl.k, dtype=torch.int32, device="cuda")
+    w = torch.zeros(1, wl.k, device="cuda")
+    out = torch.zeros(1, wl.H, device="cuda")
+    before = moe_launch_count()
+    with pytest.raises(MoeError) as e:  # resid_out is resid_in
+        moe_layer_forward_routed_resid(L.handle, r[:1], None, r[:1], u, 1e-6, wr, ids, w, out)
+    assert e.value.name == "MOE_ERR_INVALID_ARG"
+    with pytest.raises(MoeError) as e:  # delta is resid_out
+        moe_layer_forward_routed_resid(L.handle, r[:1], r[1:], r[1:], u, 1e-6, wr, ids, w, out)
+    assert e.value.name == "MOE_ERR_INVALID_ARG"
+    assert moe_launch_count() == before
