@@ -87,7 +87,7 @@ void free_layer(Layer *L) {
                   L->route_weight, L->h32, L->out_acc, L->err, L->sync, L->x16, L->h16,
                   L->tiles_ug, L->tiles_dn, L->tile_counts, L->ybuf, L->route_pos,
                   L->dense_ids, L->dense_w, L->rlog, L->x_stage, L->out_stage, L->hr,
-                  L->hsh, L->useq, L->ulog};
+                  L->hsh, L->useq, L->ulog, L->bseq, L->blog, L->bpart, L->bhq};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   if (L->tev) {
@@ -160,11 +160,16 @@ moe_status forward_impl(Layer *L, const void *x, moe_dtype xdt, int32_t T, const
     return fail(MOE_ERR_MISALIGNED, "ids/weights are not 4-byte aligned");
   if (!moe::aligned(out, 16)) return fail(MOE_ERR_MISALIGNED, "out is not 16-byte aligned");
   if (ev && !start_recorded) MOE_CUDA(rec(ev[0], st), "timing event");
-  if (moe::fused_decode_supported(*L, T)) {
+  const bool batch = moe::batch_decode_supported(*L, T);
+  if (batch || moe::fused_decode_supported(*L, T)) {
     if (ev) MOE_CUDA(rec(ev[1], st), "timing event");
-    MOE_CUDA(moe::launch_decode_fused(*L, x, xdt, T, nullptr, nullptr, 0, ids, w, nullptr, nullptr,
-                                      out, odt, st),
-             "fused decode");
+    if (batch)
+      MOE_CUDA(moe::launch_decode_batch(*L, x, xdt, T, nullptr, nullptr, 0, ids, w, nullptr, nullptr, out, odt, st),
+               "batch decode");
+    else
+      MOE_CUDA(moe::launch_decode_fused(*L, x, xdt, T, nullptr, nullptr, 0, ids, w, nullptr, nullptr,
+                                        out, odt, st),
+               "fused decode");
     if (ev) {
       MOE_CUDA(rec(ev[2], st), "timing event");
       MOE_CUDA(rec(ev[3], st), "timing event");
@@ -257,6 +262,7 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
     // kernel attributes of this device, and whether the single-launch decode
     // grid can be resident at once
     if (e0 == cudaSuccess) e0 = moe::decode_prepare(*L);
+    if (e0 == cudaSuccess && sh->max_tokens >= 2) e0 = moe::batch_decode_prepare(*L);
     if (e0 == cudaSuccess) e0 = moe::router_tc_prepare();
     if (e0 != cudaSuccess) {
       free_layer(L);
@@ -285,6 +291,12 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
     ALLOC(L->hsh, sizeof(float) * (int64_t)L->Fp);
     ALLOC(L->useq, sizeof(unsigned long long) * moe::unit_decode_seq_words());
     ALLOC(L->ulog, sizeof(unsigned long long) * (int64_t)L->sms * E);
+  }
+  if (L->batch_smem_limit > 0) {
+    ALLOC(L->bseq, sizeof(unsigned long long) * moe::batch_decode_seq_words());
+    ALLOC(L->blog, sizeof(unsigned long long) * moe::batch_decode_log_words(*L));
+    ALLOC(L->bpart, sizeof(float) * moe::batch_decode_part_floats(*L));
+    ALLOC(L->bhq, sizeof(float) * moe::batch_decode_hq_floats());
   }
   ALLOC(L->out_acc, sizeof(float) * (int64_t)sh->max_tokens * H);
   ALLOC(L->err, sizeof(unsigned));
@@ -324,6 +336,10 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
     e = cudaMemsetAsync(L->useq, 0, sizeof(unsigned long long) * moe::unit_decode_seq_words(), st);
   if (e == cudaSuccess && L->ulog)
     e = cudaMemsetAsync(L->ulog, 0, sizeof(unsigned long long) * (size_t)L->sms * E, st);
+  if (e == cudaSuccess && L->bseq)
+    e = cudaMemsetAsync(L->bseq, 0, sizeof(unsigned long long) * moe::batch_decode_seq_words(), st);
+  if (e == cudaSuccess && L->blog)
+    e = cudaMemsetAsync(L->blog, 0, sizeof(unsigned long long) * (size_t)moe::batch_decode_log_words(*L), st);
   if (e == cudaSuccess)
     e = cudaMemsetAsync(L->rlog, 0,
                         sizeof(unsigned long long) * moe::kLogitCopies * moe::kFusedMaxTokens * E, st);
@@ -343,6 +359,7 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   }
   if (e == cudaSuccess) e = moe::tc_prepare(*L);
   if (e == cudaSuccess) e = moe::gemv_prepare(*L);
+  if (e == cudaSuccess) e = moe::batch_decode_maps(*L);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {
     free_layer(L);
@@ -400,7 +417,7 @@ moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype 
     return fail(MOE_ERR_INVALID_ARG, "out_dtype %d is not MOE_DT_BF16 or MOE_DT_FP32", (int)out_dtype);
   if (T > 0 && !out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
   if (T > 0 && out && !moe::aligned(out, 16)) return fail(MOE_ERR_MISALIGNED, "out is not 16-byte aligned");
-  if (L && T > 0 && T <= L->max_tokens && moe::fused_decode_supported(*L, T)) {
+  if (L && T > 0 && T <= L->max_tokens && (moe::batch_decode_supported(*L, T) || moe::fused_decode_supported(*L, T))) {
     moe_status s = check_x(L, x, x_dtype, T);
     if (s != MOE_OK) return s;
     if (!router_w || !ids || !weights) return fail(MOE_ERR_INVALID_ARG, "router_w, ids and weights must be non-NULL");
@@ -413,9 +430,14 @@ moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype 
       MOE_CUDA(rec(ev[0], st), "timing event");
       MOE_CUDA(rec(ev[1], st), "timing event");
     }
-    MOE_CUDA(moe::launch_decode_fused(*L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, nullptr,
-                                      nullptr, ids, weights, out, out_dtype, st),
-             "fused decode");
+    if (moe::batch_decode_supported(*L, T))
+      MOE_CUDA(moe::launch_decode_batch(*L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, nullptr, nullptr,
+                                        ids, weights, out, out_dtype, st),
+               "batch decode");
+    else
+      MOE_CUDA(moe::launch_decode_fused(*L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, nullptr,
+                                        nullptr, ids, weights, out, out_dtype, st),
+               "fused decode");
     if (ev) {
       MOE_CUDA(rec(ev[2], st), "timing event");
       MOE_CUDA(rec(ev[3], st), "timing event");

@@ -34,6 +34,8 @@ constexpr int kGroupRows = 64;  // gate/up interleave group
 
 // Largest batch the single-launch decode kernel handles.
 constexpr int kFusedMaxTokens = 8;
+// Largest batch of the single-launch batch kernel (2..16 tokens).
+constexpr int kBatchMaxTokens = 16;
 // Largest batch of the batched decode path (register dequantisation + mma.sync).
 constexpr int kGemvMaxTokens = 64;
 constexpr int kLogitCopies = 8;  // copies of the decode kernel's tagged router logits
@@ -90,6 +92,12 @@ struct Layer {
   float *hsh = nullptr;      // [Fp] the shared expert's SwiGLU output
   unsigned long long *useq = nullptr;  // arrival counters (exit, shared h, h of each slot), never reset
   unsigned long long *ulog = nullptr;  // [E][sms] tagged router logits, one private copy per CTA
+  // single-launch batch kernel, 2..16 tokens (decode_batch.cu)
+  int batch_smem_limit = 0;            // its dynamic shared-memory limit; 0: the kernel is not used
+  unsigned long long *bseq = nullptr;  // exit counter, then two sets (by call parity) of per-entry counters
+  unsigned long long *blog = nullptr;  // [16][E][sms] tagged router logits, one private copy per CTA
+  float *bpart = nullptr;              // [routes][Fp][2] first-half gate and up sums
+  float *bhq = nullptr;                // [routes][32][16] quantised h words, then [routes][32] scales
   float *out_acc = nullptr;  // [max_tokens][H] fp32 accumulator
   // deterministic combine only (else nullptr)
   float *ybuf = nullptr;     // [max_routes][Hp] weighted down outputs, route order
@@ -116,6 +124,7 @@ struct Layer {
   CUtensorMap map_gu_lab, map_dn_lab;  // weight labels of one k-step
   // batched decode path (9..64 tokens)
   CUtensorMap map_gu_sb, map_dn_sb;    // one superblock column of 128 weight rows
+  CUtensorMap map_gu_half;             // half an up/gate row of 8 rows (batch kernel)
   CUtensorMap map_x16_16, map_h16_16;  // activation rows in route order, 16-row boxes
   int gemv_ready = 0;                  // the layer's shape fits the batched decode path
 };
@@ -219,6 +228,19 @@ bool fused_decode_supported(const Layer &L, int T);
 // 32-output block) units; taken by launch_decode_fused at T = 1 when the
 // layer's shape has an instance (H padded to 3,584 or 2,560).
 cudaError_t unit_decode_prepare(Layer &L);
+// Single-launch batch kernel (2..16 tokens): kernel attributes and whether
+// its grid fits (create, before the buffers), its tensor map (after the
+// weights are allocated), buffer sizes, and the launch.
+cudaError_t batch_decode_prepare(Layer &L);
+cudaError_t batch_decode_maps(Layer &L);
+int batch_decode_seq_words();
+int64_t batch_decode_hq_floats();
+int64_t batch_decode_part_floats(const Layer &L);
+int64_t batch_decode_log_words(const Layer &L);
+bool batch_decode_supported(const Layer &L, int T);
+cudaError_t launch_decode_batch(const Layer &L, const void *x, moe_dtype xdt, int T, const float *wr,
+                                const float *bias, int64_t bstride, const int32_t *ids_in, const float *w_in,
+                                int32_t *ids_out, float *w_out, void *out, moe_dtype odt, cudaStream_t stream);
 int unit_decode_seq_words();
 bool unit_decode_supported(const Layer &L);
 // The layer input of one trunk step, formed inside the one-token kernel:
