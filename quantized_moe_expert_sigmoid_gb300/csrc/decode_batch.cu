@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kBT, 1)
   __shared__ int u_grp[kBMaxUnits], u_b[kBMaxUnits];  // token group and block of each of this CTA's units
   __shared__ int grp_ent[kBMaxGroups], grp_c0[kBMaxGroups], pgroups[kBMaxPlan];
   __shared__ int n_groups_s;
-  __shared__ float red_r[kBW][kBMaxT];
+  __shared__ float red_r[kBW];
 
   const Layer &L = p.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -469,55 +469,53 @@ __global__ void __launch_bounds__(kBT, 1)
         bulk_g2s(xq + (size_t)t * xw, reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * H, rowb, &x_bar);
   }
 
-  // ---- router logits of expert my_e for every token: fp32 dots, each
-  // thread's part for all tokens, then warp partials added in warp order ----
+  // ---- router logits of expert my_e for every token: 32 / T warps per
+  // token (a short rolled loop: this code runs once per call, from a cold
+  // instruction cache), eight elements per lane and step; the warps' sums
+  // of a token are added in warp order ----
+  const int wpt = kBW / T;  // warps per token
   if (router) {
     if (p.wr_smem && !mbar_wait_ns(&wr_bar, 0, kBWaitNs)) atomicOr(&status, 2);
     if (x_smem && !mbar_wait_suspend(&x_bar, 0, kBWaitNs)) atomicOr(&status, 2);
     const float *w = p.wr_smem ? wrs : p.wr + (int64_t)my_e * H;
-    float acc[kBMaxT];
-#pragma unroll
-    for (int t = 0; t < kBMaxT; ++t) acc[t] = 0.f;
-    // eight consecutive elements per thread: every token's x loads are
-    // independent 16- or 32-byte loads (H is a multiple of 8)
-    for (int i8 = tid; i8 < H / 8; i8 += kBT) {
-      const int i = i8 * 8;
-      const float4 w0 = *reinterpret_cast<const float4 *>(w + i);
-      const float4 w1 = *reinterpret_cast<const float4 *>(w + i + 4);
-      const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-      for (int t = 0; t < kBMaxT; ++t)
-        if (t < T) {
-          float xv[8];
-          if (x_smem) {
-            const uint4 q = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(xq) + (size_t)t * xw + i);
-            const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) {
-              xv[2 * k2] = __uint_as_float(qq[k2] << 16);
-              xv[2 * k2 + 1] = __uint_as_float(qq[k2] & 0xFFFF0000u);
-            }
-          } else {
-            const float4 a = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.x) + (size_t)t * H + i);
-            const float4 b = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.x) + (size_t)t * H + i + 4);
-            xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
-            xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
-          }
-#pragma unroll
-          for (int k2 = 0; k2 < 8; ++k2) acc[t] = fmaf(xv[k2], wv[k2], acc[t]);
+    const int t = warp / wpt;
+    float acc = 0.f;
+    if (t < T) {
+#pragma unroll 1
+      for (int i8 = (warp - t * wpt) * 32 + lane; i8 < H / 8; i8 += wpt * 32) {
+        const int i = i8 * 8;
+        const float4 w0 = *reinterpret_cast<const float4 *>(w + i);
+        const float4 w1 = *reinterpret_cast<const float4 *>(w + i + 4);
+        float4 a, b;
+        if (x_smem) {
+          const uint4 q = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(xq) + (size_t)t * xw + i);
+          a = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u),
+                          __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
+          b = make_float4(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u),
+                          __uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u));
+        } else {
+          a = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.x) + (size_t)t * H + i);
+          b = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.x) + (size_t)t * H + i + 4);
         }
-    }
-#pragma unroll
-    for (int t = 0; t < kBMaxT; ++t)
-      if (t < T) {
-        const float v = bwarp_sum(acc[t]);
-        if (lane == 0) red_r[warp][t] = v;
+        acc = fmaf(a.x, w0.x, acc);
+        acc = fmaf(a.y, w0.y, acc);
+        acc = fmaf(a.z, w0.z, acc);
+        acc = fmaf(a.w, w0.w, acc);
+        acc = fmaf(b.x, w1.x, acc);
+        acc = fmaf(b.y, w1.y, acc);
+        acc = fmaf(b.z, w1.z, acc);
+        acc = fmaf(b.w, w1.w, acc);
       }
+    }
+    acc = bwarp_sum(acc);
+    if (lane == 0) red_r[warp] = acc;
   }
   __syncthreads();
-  if (router && warp * 32 < G) {  // every publishing warp adds the 32 warp partials in the same order
+  if (router && warp * 32 < G) {  // every publishing warp adds a token's warp sums in the same order
+#pragma unroll 1
     for (int t = 0; t < T; ++t) {
-      float v = bwarp_sum(red_r[lane][t]);
+      float v = 0.f;
+      for (int k = 0; k < wpt; ++k) v += red_r[t * wpt + k];
       if (p.bias && !L.sel_bias) v += p.bias[(int64_t)t * p.bstride + my_e];
       if (tid < G)
         st_relaxed_u64(&L.blog[((int64_t)t * E + my_e) * G + tid], ((unsigned long long)tag << 32) | __float_as_uint(v));
