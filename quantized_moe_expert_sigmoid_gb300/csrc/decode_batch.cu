@@ -411,6 +411,7 @@ __global__ void __launch_bounds__(kBT, 1)
   // ---- set-up; the router row and the shared expert's first stages go out
   // before the wait for the previous grid (weights are immutable) ----
   const bool pre = S && c < NB;  // this CTA's first unit is the shared expert's block c
+  const uint64_t wpol = l2_evict_first();  // expert weights: read once per call
   if (tid == 0) {
     for (int s = 0; s < kBMaxSlots; ++s) mbar_init(&full_bar[s], 1);
     mbar_init(&wr_bar, 1);
@@ -431,8 +432,9 @@ __global__ void __launch_bounds__(kBT, 1)
         uint8_t *dst = ring + (size_t)st * kStage;
         slot_stage[st] = st;
         mbar_arrive_expect_tx(&full_bar[st], (uint32_t)(2 * kBChunk * kPB));
-        tma_load_2d(dst, &gu_map, part * kBox0, row0 + kBChunk * q, &full_bar[st]);
-        tma_load_2d(dst + kBChunk * kPB, &gu_map, part * kBox0, row0 + kBChunk * q + kGroupRows, &full_bar[st]);
+        tma_load_2d_hint(dst, &gu_map, part * kBox0, row0 + kBChunk * q, &full_bar[st], wpol);
+        tma_load_2d_hint(dst + kBChunk * kPB, &gu_map, part * kBox0, row0 + kBChunk * q + kGroupRows, &full_bar[st],
+                         wpol);
       }
       issued_upto = kBPre;
     }
@@ -739,8 +741,8 @@ __global__ void __launch_bounds__(kBT, 1)
     const int iu = s >> 3, q = (s >> 1) & 3, part = s & 1;
     const int row0 = pe[grp_ent[u_grp[iu]]] * 2 * L.Fp + b_gate_row(kBUnit * u_b[iu] + kBChunk * q);
     mbar_arrive_expect_tx(bar, (uint32_t)(2 * kBChunk * kPB));
-    tma_load_2d(dst, &gu_map, part * kBox0, row0, bar);
-    tma_load_2d(dst + kBChunk * kPB, &gu_map, part * kBox0, row0 + kGroupRows, bar);
+    tma_load_2d_hint(dst, &gu_map, part * kBox0, row0, bar, wpol);
+    tma_load_2d_hint(dst + kBChunk * kPB, &gu_map, part * kBox0, row0 + kGroupRows, bar, wpol);
     atomicMax(&issued_upto, s + 1);
   };
   if (tid == 0)
@@ -876,8 +878,8 @@ __global__ void __launch_bounds__(kBT, 1)
     if (nr > 0) {
       const uint32_t bytes = (uint32_t)(nr * db);
       mbar_arrive_expect_tx(&dbar[slot], bytes);
-      bulk_g2s(dring + (size_t)slot * dstage, L.dn + (int64_t)pe[d] * L.dn_expert_bytes + (int64_t)n0 * db, bytes,
-               &dbar[slot]);
+      bulk_g2s_hint(dring + (size_t)slot * dstage, L.dn + (int64_t)pe[d] * L.dn_expert_bytes + (int64_t)n0 * db,
+                    bytes, &dbar[slot], wpol);
     } else {
       mbar_arrive(&dbar[slot]);
     }

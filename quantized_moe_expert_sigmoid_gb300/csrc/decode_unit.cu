@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
   const int n_mine = c < R ? (R - 1 - c) / G + 1 : 0;  // routed units of this CTA: c, c + G, ...
 
   uint8_t *ring = smem;
+  const uint64_t wpol = l2_evict_first();  // expert weights: read once per call
   // shared gate/up rows [nfs gate][nfs up], in the last two ring stages until
   // the shared slice is computed (a routed unit's first stages go out first)
   uint8_t *sg_rows = smem + (size_t)kUShStage * kChunk;
@@ -232,9 +233,9 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
     for (int s = s0; s < s1; ++s) {
       const uint8_t *g = base + (int64_t)(s * kUChunkOut) * kRB;
       mbar_arrive_expect_tx(&full_bar[s], (uint32_t)kChunk);
-      bulk_g2s(ring + (size_t)s * kChunk, g, (uint32_t)(kUChunkOut * kRB), &full_bar[s]);
-      bulk_g2s(ring + (size_t)s * kChunk + kUChunkOut * kRB, g + (int64_t)kGroupRows * kRB,
-               (uint32_t)(kUChunkOut * kRB), &full_bar[s]);
+      bulk_g2s_hint(ring + (size_t)s * kChunk, g, (uint32_t)(kUChunkOut * kRB), &full_bar[s], wpol);
+      bulk_g2s_hint(ring + (size_t)s * kChunk + kUChunkOut * kRB, g + (int64_t)kGroupRows * kRB,
+               (uint32_t)(kUChunkOut * kRB), &full_bar[s], wpol);
     }
   };
 
@@ -260,9 +261,9 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
       while (f < fs0 + nfs) {
         const int n = min(fs0 + nfs, (f / kGroupRows + 1) * kGroupRows) - f;
         const uint8_t *g = sgu + (int64_t)gate_row(f) * kRB;
-        bulk_g2s(sg_rows + (size_t)at * kRB, g, (uint32_t)(n * kRB), &sh_bar);
-        bulk_g2s(sg_rows + (size_t)(nfs + at) * kRB, g + (int64_t)kGroupRows * kRB, (uint32_t)(n * kRB),
-                 &sh_bar);
+        bulk_g2s_hint(sg_rows + (size_t)at * kRB, g, (uint32_t)(n * kRB), &sh_bar, wpol);
+        bulk_g2s_hint(sg_rows + (size_t)(nfs + at) * kRB, g + (int64_t)kGroupRows * kRB, (uint32_t)(n * kRB),
+                 &sh_bar, wpol);
         f += n;
         at += n;
       }
@@ -351,8 +352,8 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
     epoch_s = ld_acquire64(&L.useq[kUSeqExit]) / (unsigned long long)G;
     if (S && nr > 0) {  // the shared expert's W_down rows of this CTA's output rows
       mbar_arrive_expect_tx(&dsh_bar, (uint32_t)(nr * db));
-      bulk_g2s(dn_rows + (size_t)K * dn_slice, L.dn + (int64_t)E * L.dn_expert_bytes + (int64_t)n0 * db,
-               (uint32_t)(nr * db), &dsh_bar);
+      bulk_g2s_hint(dn_rows + (size_t)K * dn_slice, L.dn + (int64_t)E * L.dn_expert_bytes + (int64_t)n0 * db,
+               (uint32_t)(nr * db), &dsh_bar, wpol);
     }
   }
 
@@ -480,8 +481,8 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
       mbar_arrive_expect_tx(&drt_bar, bytes);
       for (int j = 0; j < K; ++j)
         if (sel_id[j] >= 0 && nr > 0)
-          bulk_g2s(dn_rows + (size_t)j * dn_slice, L.dn + (int64_t)sel_id[j] * L.dn_expert_bytes + (int64_t)n0 * db,
-                   (uint32_t)(nr * db), &drt_bar);
+          bulk_g2s_hint(dn_rows + (size_t)j * dn_slice, L.dn + (int64_t)sel_id[j] * L.dn_expert_bytes + (int64_t)n0 * db,
+                   (uint32_t)(nr * db), &drt_bar, wpol);
     }
   } else {
     // ---- x to 16-bit integers per 32-block: four threads per block, eight
