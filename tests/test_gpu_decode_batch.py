@@ -132,3 +132,29 @@ def test_batch_is_bit_reproducible():
         outs.append(o.clone())
     L.check()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+@pytest.mark.parametrize("T", [4, 13])
+def test_fp32_activations_and_a_shared_bias_row(T):
+    """fp32 x (bf16 values exactly, so routing is unchanged) takes the
+    kernel's path that reads x from global memory; a single [E] logit bias
+    row applies to every token; the bf16 output is the fp32 one rounded once."""
+    wl, ew, L = _layer("decode1")
+    c = cases.make_case(wl, T=T, ew=ew, seed=10)
+    x32 = torch.from_numpy(synth.bf16_bits_to_f32(c.x).reshape(T, wl.H)).cuda()
+    wr = torch.from_numpy(c.wr).cuda()
+    row = np.zeros(wl.E, np.float32)
+    row[int(np.argsort(-c.logits[0], kind="stable")[wl.k])] = 3.0  # token 0's best unselected expert
+    out, ids, w = L.forward_routed(x32, wr, torch.from_numpy(row).cuda(), out_dtype=torch.float32)
+    L.check()
+    ref_ids, ref_w, logits = oracle.route(c.x64, c.wr, wl.k, wl.scale, row)
+    clear = oracle.min_topk_gap(logits, wl.k) >= 1e-4
+    assert clear.sum() >= T - 1
+    ids_g, w_g = ids.cpu().numpy(), w.cpu().numpy()
+    np.testing.assert_array_equal(ids_g[clear], ref_ids[clear])
+    np.testing.assert_allclose(w_g[clear], ref_w[clear], rtol=0, atol=2e-6)
+    ref = parity.oracle_forward(c.x64, ids_g, w_g.astype(np.float64), ew)
+    parity.assert_close_fp32(out.cpu().numpy(), ref, f"fp32 x T={T}")
+    out_b, _, _ = L.forward_routed(x32, wr, torch.from_numpy(row).cuda(), out_dtype=torch.bfloat16)
+    L.check()
+    np.testing.assert_array_equal(out_b.float().cpu().numpy(), out.to(torch.bfloat16).float().cpu().numpy())
