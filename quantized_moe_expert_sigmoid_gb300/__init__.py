@@ -121,10 +121,16 @@ def _ptr(t, name="tensor", dtypes=None):
     return ctypes.c_void_p(t.data_ptr())
 
 
+_DT = None
+
+
 def _dt():
-    import torch
-    return {"x": (torch.bfloat16, torch.float32), "f32": (torch.float32,),
-            "i32": (torch.int32,), "u8": (torch.uint8,)}
+    global _DT
+    if _DT is None:  # (built once: the marshalling runs on every call)
+        import torch
+        _DT = {"x": (torch.bfloat16, torch.float32), "f32": (torch.float32,),
+               "i32": (torch.int32,), "u8": (torch.uint8,)}
+    return _DT
 
 
 def _dtype(t) -> int:

@@ -474,11 +474,13 @@ moe_status moe_layer_forward_routed_host(moe_layer_t layer, const void *x_host, 
   if (!x_host || !out_host) return fail(MOE_ERR_INVALID_ARG, "x_host and out_host must be non-NULL");
   cudaStream_t st = (cudaStream_t)stream;
   const size_t n = (size_t)T * L->H;
-  // Batches the single-launch decode kernel runs read x and write out
-  // through the host buffers themselves when the device can address them
-  // (page-locked memory; on GB300 over the NVLink-C2C link to the Grace
-  // host), so a step is one launch and no copy-engine round trips.
-  if (moe::fused_decode_supported(*L, T)) {
+  // One token on the one-token kernel reads x and writes out through the
+  // host buffers themselves when the device can address them (page-locked
+  // memory; on GB300 over the NVLink-C2C link to the Grace host), so a step
+  // is one launch and no copy-engine round trips.  Larger batches are copied
+  // in once: their kernels have every CTA read the whole of x, which over the
+  // host link would be one read of x per CTA.
+  if (T == 1 && moe::unit_decode_supported(*L)) {
     void *xd = device_view(x_host), *od = device_view(out_host);
     if (xd && od && moe::aligned(xd, 16) && moe::aligned(od, 16))
       return moe_layer_forward_routed(layer, xd, x_dtype, T, router_w, logit_bias, bias_row_stride, ids,
