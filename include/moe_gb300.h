@@ -111,12 +111,14 @@ typedef struct {
 
 /* Deterministic combine [PocketLLM, "Xing4.0-29B-A4B: the design record",
  * section 4: float atomics make the top-k sum differ from run to run].
- * Batches above 8 tokens then store each route's weighted down output once
- * (no atomics) and add a token's routes in slot order, the shared expert
- * last, so equal inputs give equal output bits on every call.  It costs an
- * extra [routes][H] fp32 buffer (max_tokens * (top_k + n_shared) rows,
- * allocated at create) and one write and one read of it per call.  Batches
- * of up to 8 tokens are deterministic with or without the flag. */
+ * Batches on the multi-launch paths (above 16 tokens, or above 8 for shapes
+ * the batch kernel does not take) then store each route's weighted down
+ * output once (no atomics) and add a token's routes in slot order, the
+ * shared expert last, so equal inputs give equal output bits on every call.
+ * It costs an extra [routes][H] fp32 buffer (max_tokens * (top_k +
+ * n_shared) rows, allocated at create) and one write and one read of it per
+ * call.  The single-launch decode kernels (up to 16 tokens) are
+ * deterministic with or without the flag. */
 #define MOE_FLAG_DETERMINISTIC 2u
 
 /* Host input and output for moe_layer_forward_routed_host: the layer holds
