@@ -409,8 +409,10 @@ def measure_layer(args, name, steps, warmup, world, rank, local_rank, dev, cpu_s
         kname = "whole trunk step (every layer's calls and the residual RMSNorm launches)"
     elif T == 1:
         kname = "decode_unit_kernel (the step's only launch)"
-    elif T <= 16:
+    elif T <= 16 and wl.H in (3584, 2560):
         kname = "decode_batch_kernel (the step's only launch)"
+    elif T <= 8:
+        kname = "decode_fused_kernel (the step's only launch)"
     else:
         kname = "whole layer call (all launches of one step)"
     roofline = {"bound": "hbm",
