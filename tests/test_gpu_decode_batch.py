@@ -158,3 +158,26 @@ def test_fp32_activations_and_a_shared_bias_row(T):
     out_b, _, _ = L.forward_routed(x32, wr, torch.from_numpy(row).cuda(), out_dtype=torch.bfloat16)
     L.check()
     np.testing.assert_array_equal(out_b.float().cpu().numpy(), out.to(torch.bfloat16).float().cpu().numpy())
+
+
+@pytest.mark.parametrize("H,E,k,F,T,S", [(3488, 40, 3, 992, 6, 1), (2528, 100, 8, 736, 11, 0)])
+def test_ragged_shapes_on_the_batch_kernel(H, E, k, F, T, S):
+    """H and F that are not multiples of 256 (x copied row by row, the pad
+    columns read as zero; padded outputs with zero weights), an odd expert
+    count, k = 3 and k = 8, with and without the shared expert: one launch,
+    ids bit for bit, output within tolerance."""
+    wl = synth.Workload("ragged batch", H, E, k, F, T, "bf16", 1.2 / H ** 0.5, n_shared=S)
+    ew = synth.expert_weights(13, 0, E, H, F, S)
+    if not S:
+        ew.sh_up = ew.sh_gate = ew.sh_down = None
+    c = cases.make_case(wl, seed=13, ew=ew)
+    L = MoeLayer.from_weights(ew, k=k, scale=2.0, max_tokens=16)
+    x, wr = _inputs(c)
+    before = moe_launch_count()
+    out, ids, w = L.forward_routed(x, wr, out_dtype=torch.float32)
+    assert moe_launch_count() - before == 1
+    L.check()
+    np.testing.assert_array_equal(ids.cpu().numpy(), c.ids)
+    ref = parity.oracle_forward(c.x64, c.ids, c.w, ew)
+    parity.assert_close_fp32(out.cpu().numpy(), ref, f"H{H} E{E} k{k} F{F} T{T}")
+    L.close()
