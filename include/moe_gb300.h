@@ -126,6 +126,18 @@ typedef struct {
  * bytes, allocated at create. */
 #define MOE_FLAG_HOST_IO 4u
 
+/* Cooperative launches for the single-launch decode kernels (up to 16
+ * tokens), which hold one CTA on every SM and wait device-wide inside.  At
+ * create the layer checks that one CTA fits on every SM; without this flag
+ * the kernels are plain launches (a cooperative launch adds about 3 us of
+ * launch latency to every call that is not replayed from a CUDA graph), so
+ * a caller must not keep SMs busy with other kernels, on other streams or
+ * through MPS or green contexts, while a decode call runs: its waits would
+ * run out and the call would report MOE_ERR_TIMEOUT.  With the flag the
+ * runtime starts each such launch only once its whole grid can be resident
+ * at the same time. */
+#define MOE_FLAG_COOPERATIVE 8u
+
 /* Expert weights in IQ4_NL blocks (18 bytes each, no alignment needed).
  *   up, gate: [E][F][H/32] blocks     down: [E][H][F/32] blocks
  *   sh_up, sh_gate: [F][H/32]         sh_down: [H][F/32]  (NULL if no shared)
@@ -198,11 +210,11 @@ moe_status moe_route(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_
  * is graph-capturable.  The single-launch decode kernels (T <= 8; T = 1 has
  * its own, which splits the routed experts into 32-output units, one per SM)
  * hold every SM of the device for the duration of the call and wait
- * device-wide inside, so they are launched as cooperative launches: the runtime starts it
- * only once its whole grid can be resident, and refuses it (MOE_ERR_CUDA,
- * "too many blocks in cooperative launch") when the device cannot hold the
- * grid at all.  Its waits are bounded as well; one that gives up is reported
- * by moe_layer_check() as MOE_ERR_TIMEOUT. */
+ * device-wide inside: a layer whose grid of one CTA per SM cannot be
+ * resident takes the multi-launch path (checked at create), and with
+ * MOE_FLAG_COOPERATIVE the runtime starts each launch only once its whole
+ * grid can be resident.  Their waits are bounded; one that gives up is
+ * reported by moe_layer_check() as MOE_ERR_TIMEOUT. */
 moe_status moe_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
                        const int32_t *ids, const float *weights, void *out,
                        moe_dtype out_dtype, void *stream);

@@ -21,6 +21,7 @@ MOE_DT_FP32 = 1
 MOE_FLAG_SELECTION_BIAS = 1  # the bias ranks experts only (noaux_tc); weights stay unbiased
 MOE_FLAG_DETERMINISTIC = 2   # slot-ordered combine: equal inputs give equal output bits
 MOE_FLAG_HOST_IO = 4         # device copy buffers for moe_layer_forward_routed_host
+MOE_FLAG_COOPERATIVE = 8     # cooperative launches for the single-launch decode kernels
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_OUT_OF_MEMORY", 5: "MOE_ERR_CUDA",

@@ -231,7 +231,7 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   if (S != 0 && S != 1) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "n_shared = %d: need 0 or 1", S);
   if (!(sh->routed_scaling > 0.f)) return fail(MOE_ERR_INVALID_ARG, "routed_scaling must be > 0");
   if (sh->max_tokens < 1 || sh->max_tokens > 65536) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "max_tokens = %d: need 1..65536", sh->max_tokens);
-  if (sh->flags & ~(MOE_FLAG_SELECTION_BIAS | MOE_FLAG_DETERMINISTIC | MOE_FLAG_HOST_IO))
+  if (sh->flags & ~(MOE_FLAG_SELECTION_BIAS | MOE_FLAG_DETERMINISTIC | MOE_FLAG_HOST_IO | MOE_FLAG_COOPERATIVE))
     return fail(MOE_ERR_INVALID_ARG, "flags = 0x%x: unknown bits", sh->flags);
   if (!wt->up || !wt->gate || !wt->down) return fail(MOE_ERR_INVALID_ARG, "up, gate and down must be non-NULL");
   if (S && (!wt->sh_up || !wt->sh_gate || !wt->sh_down)) return fail(MOE_ERR_INVALID_ARG, "shared expert weights must be non-NULL when n_shared = 1");
@@ -246,6 +246,7 @@ moe_status moe_layer_create(const moe_shapes *sh, const moe_weights *wt, void *s
   L->scale = sh->routed_scaling;
   L->sel_bias = (sh->flags & MOE_FLAG_SELECTION_BIAS) ? 1 : 0;
   L->deterministic = (sh->flags & MOE_FLAG_DETERMINISTIC) ? 1 : 0;
+  L->coop = (sh->flags & MOE_FLAG_COOPERATIVE) ? 1 : 0;
   L->max_tokens = sh->max_tokens;
   L->Hp = (int)round_up(H, moe::kSBW);
   L->Fp = (int)round_up(F, moe::kSBW);

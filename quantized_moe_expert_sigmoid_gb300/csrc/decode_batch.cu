@@ -1056,16 +1056,16 @@ cudaError_t batch_launch(const BParams &p, const CUtensorMap &map, size_t smem, 
   cfg.blockDim = dim3(kBT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  // cooperative: refused unless every CTA can be resident at once (the
-  // counter waits need it); programmatic serialization: the next call's
-  // launch overlaps this call's tail
+  // programmatic serialization: the next call's launch overlaps this call's
+  // tail; cooperative (on request): started only once every CTA can be
+  // resident at once, which the counter waits need
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeCooperative;
   attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = p.L.coop ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, decode_batch_kernel<NSB, NL>, p, map);
 }
 

@@ -1026,17 +1026,16 @@ cudaError_t launch_tt(const Params &p, int grid, size_t smem, cudaStream_t strea
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  // cooperative: the runtime refuses the launch (cudaErrorCooperativeLaunchTooLarge)
-  // unless every CTA of the grid can be resident at once, which the
-  // device-wide waits inside need; programmatic serialization: the next
-  // call's prologue overlaps this call's tail
+  // programmatic serialization: the next call's prologue overlaps this
+  // call's tail; cooperative (on request): started only once every CTA of
+  // the grid can be resident at once, which the device-wide waits need
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeCooperative;
   attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = p.L.coop ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, decode_fused_kernel<TT, NP, NPD>, p);
 }
 

@@ -29,8 +29,9 @@
 // x 4 experts = 128 units of 129 KB of gate/up rows, 24 rows x 576 B of each
 // W_down per CTA, and the shared expert.
 //
-// Grid: one CTA per SM, 32 warps, cooperative: every CTA is resident, which
-// the counter waits need.  Counters and logit tags are never reset: each
+// Grid: one CTA per SM, 32 warps; the counter waits need every CTA resident
+// (checked at create: one CTA fits on every SM; with MOE_FLAG_COOPERATIVE
+// the launch is cooperative).  Counters and logit tags are never reset: each
 // counter only grows (a fixed number of arrivals per call), the call's epoch
 // is the exit counter / G read at the start (no CTA of this call has exited
 // yet), and a logit word is current when its tag is epoch + 1.
@@ -184,6 +185,7 @@ __device__ __forceinline__ void upgate_part(const uint8_t *rowg, const uint8_t *
 template <int NSB, int NL>
 __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
   static_assert(NSB % 2 == 0, "two superblocks per warp step");
+  static_assert(NSB * 256 <= kUMaxH, "bf16 x fits the x buffer");
   constexpr int kHp = NSB * 256;
   constexpr int kRB = NSB * kSBBytes;           // bytes of one up/gate row
   constexpr int kChunk = 2 * kUChunkOut * kRB;  // 4 gate rows, then their 4 up rows
@@ -270,8 +272,9 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
     }
   }
   __syncthreads();
-  // every CTA of this grid is resident (cooperative launch): the next grid
-  // may be scheduled now; it waits for this one to finish before it reads
+  // the next grid starts once every CTA of this one has passed this point
+  // (so all of them hold their SMs already); it waits for this one to
+  // finish before it reads
   pdl_launch_dependents();
   pdl_wait();  // x, the outputs and the counters may belong to the previous grid
 
@@ -355,6 +358,19 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
       bulk_g2s_hint(dn_rows + (size_t)K * dn_slice, L.dn + (int64_t)E * L.dn_expert_bytes + (int64_t)n0 * db,
                (uint32_t)(nr * db), &dsh_bar, wpol);
     }
+  }
+
+  // ---- bf16 x to shared memory, one 16-byte load per thread, all in flight
+  // together: one round trip per CTA where the router's strided reads and
+  // the quantisation's reads would each wait for their own (x may be
+  // page-locked host memory read over the host link) ----
+  if (!p.rs.r_in && xbf) {
+    const uint16_t *xg = static_cast<const uint16_t *>(p.x);
+    for (int i = tid; i < H / 8; i += kUT)
+      *reinterpret_cast<uint4 *>(xs_s + 8 * i) = *reinterpret_cast<const uint4 *>(xg + 8 * i);
+    for (int i = H / 8 * 8 + tid; i < H; i += kUT) xs_s[i] = xg[i];
+    __syncthreads();
+    xsrc = xs_s;
   }
 
   // ---- router logit of expert my_e: fp32 dot, warp partials added in warp
@@ -733,16 +749,16 @@ cudaError_t unit_launch(const UParams &p, int grid, cudaStream_t stream) {
   cfg.blockDim = dim3(kUT);
   cfg.dynamicSmemBytes = unit_smem<NSB>(p.L);
   cfg.stream = stream;
-  // cooperative: refused unless every CTA can be resident at once (the
-  // counter waits need it); programmatic serialization: the next call's
-  // launch overlaps this call's tail
+  // programmatic serialization: the next call's launch overlaps this call's
+  // tail; cooperative (on request): started only once every CTA can be
+  // resident at once, which the counter waits need
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeCooperative;
   attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = p.L.coop ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, decode_unit_kernel<NSB, NL>, p);
 }
 

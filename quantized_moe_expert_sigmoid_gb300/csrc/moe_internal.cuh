@@ -67,6 +67,7 @@ struct Layer {
   float scale;
   int sel_bias;              // 1: the bias shifts expert selection only (MOE_FLAG_SELECTION_BIAS)
   int deterministic;         // 1: slot-ordered combine, no float atomics (MOE_FLAG_DETERMINISTIC)
+  int coop;                  // 1: the single-launch decode kernels launch cooperatively (MOE_FLAG_COOPERATIVE)
   int max_tokens;
   int Hp, Fp;                // H and F padded to multiples of 256
   int64_t gu_row_bytes;      // Hp/256 * 144

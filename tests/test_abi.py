@@ -68,7 +68,7 @@ def _create(lib, **over):
     (dict(hidden=250), 2), (dict(hidden=0), 2), (dict(expert_ffn=48 + 1), 2),
     (dict(n_experts=0), 2), (dict(n_experts=300), 2), (dict(top_k=9), 2),
     (dict(top_k=9, n_experts=8), 2), (dict(n_shared=2), 2), (dict(max_tokens=0), 2),
-    (dict(routed_scaling=0.0), 1), (dict(flags=8), 1), (dict(flags=0x80000001), 1), ({}, 1)])
+    (dict(routed_scaling=0.0), 1), (dict(flags=16), 1), (dict(flags=0x80000001), 1), ({}, 1)])
 def test_create_validates_before_touching_the_gpu(lib, over, status):
     st, handle = _create(lib, **over)
     assert st == status, moe.moe_last_error()
@@ -78,7 +78,7 @@ def test_create_validates_before_touching_the_gpu(lib, over, status):
         assert "flags" in moe.moe_last_error()
 
 
-@pytest.mark.parametrize("flags", [1, 2, 3, 4, 7])
+@pytest.mark.parametrize("flags", [1, 2, 3, 4, 7, 8, 15])
 def test_known_flags_are_accepted(lib, flags):
     # known flags pass the flags check and fail later, on the NULL weights
     st, handle = _create(lib, flags=flags)
@@ -116,6 +116,6 @@ def test_stage_timing_argument_checks(lib):
 
 def test_flag_constants_match_the_header():
     src = (pathlib.Path(__file__).resolve().parents[1] / "include" / "moe_gb300.h").read_text()
-    for name in ("MOE_FLAG_SELECTION_BIAS", "MOE_FLAG_DETERMINISTIC", "MOE_FLAG_HOST_IO"):
+    for name in ("MOE_FLAG_SELECTION_BIAS", "MOE_FLAG_DETERMINISTIC", "MOE_FLAG_HOST_IO", "MOE_FLAG_COOPERATIVE"):
         m = re.search(r"#define\s+%s\s+(\d+)u" % name, src)
         assert m and int(m.group(1)) == getattr(moe, name), name

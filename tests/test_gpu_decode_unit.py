@@ -13,7 +13,7 @@ torch = pytest.importorskip("torch")
 
 import oracle
 from oracle import cases
-from quantized_moe_expert_sigmoid_gb300 import MoeError, MoeLayer, moe_launch_count, synth
+from quantized_moe_expert_sigmoid_gb300 import MOE_FLAG_COOPERATIVE, MoeError, MoeLayer, moe_launch_count, synth
 from tests import parity
 
 pytestmark = pytest.mark.gpu
@@ -152,3 +152,32 @@ def test_residual_step_rejects_overlap():
         moe_layer_forward_routed_resid(L.handle, r[:1], r[1:], r[1:], u, 1e-6, wr, ids, w, out)
     assert e.value.name == "MOE_ERR_INVALID_ARG"
     assert moe_launch_count() == before
+
+
+@pytest.mark.parametrize("name,T", [("decode1", 1), ("decode1", 4), ("tiny", 3)])
+def test_cooperative_flag_gives_the_same_bits(name, T):
+    """MOE_FLAG_COOPERATIVE changes only how the single-launch kernels are
+    launched (the one-token kernel at T = 1, the batch kernel at 4 tokens,
+    the multi-token kernel on a small hidden size): one launch each, and the
+    same ids, weights and output bits as the layer without it."""
+    wl = synth.WORKLOADS[name]
+    ew = parity.weights(0, 0, wl.E, wl.H, wl.F, 1)
+    c = cases.make_case(wl, T=T, ew=ew, seed=21)
+    if wl.x_dtype == "fp32":
+        x = torch.from_numpy(c.x).cuda()
+    else:
+        x = torch.from_numpy(c.x.view(np.int16)).cuda().view(torch.bfloat16)
+    wr = torch.from_numpy(c.wr).cuda()
+    res = []
+    for flags in (0, MOE_FLAG_COOPERATIVE):
+        L = MoeLayer.from_weights(ew, k=wl.k, scale=wl.scale, max_tokens=8, flags=flags)
+        before = moe_launch_count()
+        out, ids, w = L.forward_routed(x, wr, out_dtype=torch.float32)
+        assert moe_launch_count() - before == 1
+        L.check()
+        res.append((out.cpu(), ids.cpu(), w.cpu()))
+        L.close()
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+    np.testing.assert_array_equal(res[0][1].numpy(), c.ids)
+    parity.assert_close_fp32(res[0][0].numpy(), parity.oracle_forward(c.x64, c.ids, c.w, ew), f"{name} T={T}")
