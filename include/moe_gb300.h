@@ -243,13 +243,15 @@ moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype 
 /* moe_layer_forward_routed with x and out in host memory, for a layer
  * created with MOE_FLAG_HOST_IO: one call moves x (T * hidden elements of
  * x_dtype) to the device, runs the layer, and moves out back, all enqueued
- * on `stream`.  For one token, when the device can address both host
- * buffers directly (page-locked or registered memory, 16-byte aligned; on
- * GB300 over the NVLink-C2C link to the Grace host), the one-token kernel
- * reads x and writes out through them and no copy is enqueued; otherwise
- * (and for every larger batch, whose kernels read all of x in every CTA) x
- * and out go through the layer's device buffers with cudaMemcpyAsync
- * (page-locked buffers keep those copies asynchronous).  Either way x_host and out_host must stay valid and
+ * on `stream`.  When the device can address a host buffer directly
+ * (page-locked or registered memory, 16-byte aligned; on GB300 over the
+ * NVLink-C2C link to the Grace host) and the call runs on a single-launch
+ * decode kernel (up to 16 tokens), the kernel writes out through it, and at
+ * one token the one-token kernel also reads x there, so no copy is
+ * enqueued.  Otherwise x (for larger batches always: their kernels read all
+ * of x in every CTA) and out go through the layer's device buffers with
+ * cudaMemcpyAsync (page-locked buffers keep those copies asynchronous).
+ * Either way x_host and out_host must stay valid and
  * untouched until the stream has passed the call.  router_w,
  * logit_bias, ids and weights are device pointers as for
  * moe_layer_forward_routed.  MOE_ERR_INVALID_ARG for a layer without the

@@ -475,23 +475,30 @@ moe_status moe_layer_forward_routed_host(moe_layer_t layer, const void *x_host, 
   if (!x_host || !out_host) return fail(MOE_ERR_INVALID_ARG, "x_host and out_host must be non-NULL");
   cudaStream_t st = (cudaStream_t)stream;
   const size_t n = (size_t)T * L->H;
-  // One token on the one-token kernel reads x and writes out through the
-  // host buffers themselves when the device can address them (page-locked
-  // memory; on GB300 over the NVLink-C2C link to the Grace host), so a step
-  // is one launch and no copy-engine round trips.  Larger batches are copied
-  // in once: their kernels have every CTA read the whole of x, which over the
-  // host link would be one read of x per CTA.
-  if (T == 1 && moe::unit_decode_supported(*L)) {
-    void *xd = device_view(x_host), *od = device_view(out_host);
-    if (xd && od && moe::aligned(xd, 16) && moe::aligned(od, 16))
+  // The single-launch decode kernels (up to 16 tokens) store each output
+  // element once, so they write out through the host buffer itself when the
+  // device can address it (page-locked memory; on GB300 over the NVLink-C2C
+  // link to the Grace host): no copy-engine round trip after the kernel.
+  // One token on the one-token kernel also reads x there, so a step is one
+  // launch.  Larger batches copy x in once: their kernels have every CTA read
+  // the whole of x, which over the host link would be one read of x per CTA.
+  void *od = nullptr;
+  if (moe::batch_decode_supported(*L, T) || moe::fused_decode_supported(*L, T)) {
+    od = device_view(out_host);
+    if (od && !moe::aligned(od, 16)) od = nullptr;
+  }
+  if (od && T == 1 && moe::unit_decode_supported(*L)) {
+    void *xd = device_view(x_host);
+    if (xd && moe::aligned(xd, 16))
       return moe_layer_forward_routed(layer, xd, x_dtype, T, router_w, logit_bias, bias_row_stride, ids,
                                       weights, od, out_dtype, stream);
   }
   MOE_CUDA(cudaMemcpyAsync(L->x_stage, x_host, n * (x_dtype == MOE_DT_BF16 ? 2 : 4), cudaMemcpyHostToDevice, st),
            "copy x to the device");
   const moe_status s = moe_layer_forward_routed(layer, L->x_stage, x_dtype, T, router_w, logit_bias,
-                                                bias_row_stride, ids, weights, L->out_stage, out_dtype, stream);
-  if (s != MOE_OK) return s;
+                                                bias_row_stride, ids, weights, od ? od : L->out_stage, out_dtype,
+                                                stream);
+  if (s != MOE_OK || od) return s;
   MOE_CUDA(cudaMemcpyAsync(out_host, L->out_stage, n * (out_dtype == MOE_DT_BF16 ? 2 : 4),
                            cudaMemcpyDeviceToHost, st),
            "copy out to the host");

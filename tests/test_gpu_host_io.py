@@ -1,7 +1,9 @@
 """moe_layer_forward_routed_host: x and out in pinned host memory, the copies
 enqueued with the layer call.  Its output must equal the device-memory call's
-bit for bit (the same kernels run on the same values), for the single-launch
-decode kernel and the batched path, bf16 and fp32 out."""
+bit for bit (the same kernels run on the same values), for the one-token
+kernel (x and out through the host mapping), the batch kernel (x copied in,
+out through the host mapping) and the multi-launch path (both copied), bf16
+and fp32 out."""
 import numpy as np
 import pytest
 
@@ -15,7 +17,7 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("T", [1, 5, 64])
+@pytest.mark.parametrize("T", [1, 5, 16, 64])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 def test_host_call_equals_device_call(T, out_dtype):
     wl = synth.WORKLOADS["decode1"]
