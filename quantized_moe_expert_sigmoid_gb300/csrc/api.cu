@@ -408,10 +408,12 @@ moe_status moe_dense_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype
   return r;
 }
 
-moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype x_dtype,
-                                    int32_t T, const float *router_w, const float *logit_bias,
-                                    int64_t bias_row_stride, int32_t *ids, float *weights,
-                                    void *out, moe_dtype out_dtype, void *stream) {
+// moe_layer_forward_routed; x_import as for launch_decode_fused (the
+// host-buffer call passes it at one token, nullptr otherwise)
+static moe_status forward_routed_impl(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
+                                      const float *router_w, const float *logit_bias, int64_t bias_row_stride,
+                                      int32_t *ids, float *weights, void *out, moe_dtype out_dtype, void *stream,
+                                      void *x_import) {
   Layer *L = reinterpret_cast<Layer *>(layer);
   cudaStream_t st = (cudaStream_t)stream;
   if (out_dtype != MOE_DT_BF16 && out_dtype != MOE_DT_FP32)
@@ -437,7 +439,7 @@ moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype 
                "batch decode");
     else
       MOE_CUDA(moe::launch_decode_fused(*L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, nullptr,
-                                        nullptr, ids, weights, out, out_dtype, st),
+                                        nullptr, ids, weights, out, out_dtype, st, x_import),
                "fused decode");
     if (ev) {
       MOE_CUDA(rec(ev[2], st), "timing event");
@@ -454,6 +456,14 @@ moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype 
   s = forward_impl(L, x, x_dtype, T, ids, weights, out, out_dtype, st, ev, true);
   if (s == MOE_OK && ev) timing_advance(L);
   return s;
+}
+
+moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype x_dtype,
+                                    int32_t T, const float *router_w, const float *logit_bias,
+                                    int64_t bias_row_stride, int32_t *ids, float *weights,
+                                    void *out, moe_dtype out_dtype, void *stream) {
+  return forward_routed_impl(layer, x, x_dtype, T, router_w, logit_bias, bias_row_stride, ids, weights, out,
+                             out_dtype, stream, nullptr);
 }
 
 moe_status moe_layer_forward_routed_host(moe_layer_t layer, const void *x_host, moe_dtype x_dtype,
@@ -479,9 +489,11 @@ moe_status moe_layer_forward_routed_host(moe_layer_t layer, const void *x_host, 
   // element once, so they write out through the host buffer itself when the
   // device can address it (page-locked memory; on GB300 over the NVLink-C2C
   // link to the Grace host): no copy-engine round trip after the kernel.
-  // One token on the one-token kernel also reads x there, so a step is one
-  // launch.  Larger batches copy x in once: their kernels have every CTA read
-  // the whole of x, which over the host link would be one read of x per CTA.
+  // One token on the one-token kernel also takes x from there, so a step is
+  // one launch: bf16 x crosses the link once, each CTA bringing its share
+  // into the layer's device buffer (every CTA needs all of x; 152 reads of
+  // it over the link cost 5 us more per call); fp32 x is read by every CTA.
+  // Larger batches copy x in once: T x 7 KB per CTA is too much for the link.
   void *od = nullptr;
   if (moe::batch_decode_supported(*L, T) || moe::fused_decode_supported(*L, T)) {
     od = device_view(out_host);
@@ -490,8 +502,8 @@ moe_status moe_layer_forward_routed_host(moe_layer_t layer, const void *x_host, 
   if (od && T == 1 && moe::unit_decode_supported(*L)) {
     void *xd = device_view(x_host);
     if (xd && moe::aligned(xd, 16))
-      return moe_layer_forward_routed(layer, xd, x_dtype, T, router_w, logit_bias, bias_row_stride, ids,
-                                      weights, od, out_dtype, stream);
+      return forward_routed_impl(layer, xd, x_dtype, T, router_w, logit_bias, bias_row_stride, ids, weights, od,
+                                 out_dtype, stream, x_dtype == MOE_DT_BF16 ? L->x_stage : nullptr);
   }
   MOE_CUDA(cudaMemcpyAsync(L->x_stage, x_host, n * (x_dtype == MOE_DT_BF16 ? 2 : 4), cudaMemcpyHostToDevice, st),
            "copy x to the device");

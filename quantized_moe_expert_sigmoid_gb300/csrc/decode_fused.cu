@@ -1066,11 +1066,12 @@ bool fused_decode_supported(const Layer &L, int T) {
 cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, int T,
                                 const float *wr, const float *bias, int64_t bstride,
                                 const int32_t *ids_in, const float *w_in, int32_t *ids_out,
-                                float *w_out, void *out, moe_dtype odt, cudaStream_t stream) {
+                                float *w_out, void *out, moe_dtype odt, cudaStream_t stream, void *x_import) {
   FusedPlan fp;
   if (!plan_fused(L, T, fp)) return cudaErrorInvalidConfiguration;
   if (T == 1 && unit_decode_supported(L))
-    return launch_decode_unit(L, x, xdt, wr, bias, ids_in, w_in, ids_out, w_out, out, odt, stream);
+    return launch_decode_unit(L, x, xdt, wr, bias, ids_in, w_in, ids_out, w_out, out, odt, stream, nullptr,
+                              x_import);
   Params p;
   p.L = L;
   p.x = x;

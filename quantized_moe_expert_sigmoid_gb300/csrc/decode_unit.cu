@@ -68,8 +68,8 @@ constexpr uint32_t kUSpin = 1u << 21;   // counter polls before giving up (each 
 constexpr uint64_t kUWaitNs = 500000000ull;
 
 // useq words: [0] exits (G per call), [1] shared-expert h (G per call),
-// [2 + j] slot j's h (NB per call)
-constexpr int kUSeqExit = 0, kUSeqShared = 1, kUSeqSlot0 = 2;
+// [2 + j] slot j's h (NB per call), [2 + kUMaxK] x imported (G per call)
+constexpr int kUSeqExit = 0, kUSeqShared = 1, kUSeqSlot0 = 2, kUSeqX = kUSeqSlot0 + kUMaxK;
 
 struct UParams {
   Layer L;
@@ -84,6 +84,7 @@ struct UParams {
   int out_bf16;
   int wr_smem;  // 1: the router row is bulk-copied into shared memory
   ResidStep rs;  // rs.r_in != nullptr: x is formed from the residual stream here
+  uint16_t *x_import;  // non-null: bf16 x is host memory, brought into this device buffer first
   int nr_max;   // largest output-row slice of a CTA (sizes the W_down row region)
 };
 
@@ -95,6 +96,9 @@ __device__ __forceinline__ float uwarp_sum(float v) {
 
 __device__ __forceinline__ void red_release_add64(unsigned long long *p, unsigned long long v) {
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void red_relaxed_add64(unsigned long long *p, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long *p) {
   unsigned long long v;
@@ -360,14 +364,35 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
     }
   }
 
+  // ---- x in host memory (the host-buffer call): every CTA copies its share
+  // of x's 16-byte chunks into a device buffer and reads x from there once
+  // every CTA has, so x crosses the host link once per call instead of once
+  // per CTA.  Every launch adds one arrival per CTA, imported or not (a
+  // launch without an import adds it on the way out), so the counter's
+  // target follows the call epoch ----
+  if (p.x_import) {
+    const unsigned nch = (unsigned)H / 8u;
+    const int q0 = (int)((unsigned)c * nch / uG), q1 = (int)((unsigned)(c + 1) * nch / uG);
+    if (tid < q1 - q0)
+      reinterpret_cast<uint4 *>(p.x_import)[q0 + tid] = reinterpret_cast<const uint4 *>(p.x)[q0 + tid];
+    __syncthreads();
+    if (tid == 0) {
+      red_release_add64(&L.useq[kUSeqX], 1ull);
+      if (!spin_until_geq64(&L.useq[kUSeqX], (epoch_s + 1) * (unsigned long long)G)) {
+        atomicOr(&status, 1);
+        atomicOr(L.err, kErrTimeout);
+      }
+    }
+    __syncthreads();
+  }
+
   // ---- bf16 x to shared memory, one 16-byte load per thread, all in flight
   // together: one round trip per CTA where the router's strided reads and
-  // the quantisation's reads would each wait for their own (x may be
-  // page-locked host memory read over the host link) ----
+  // the quantisation's reads would each wait for their own ----
   if (!p.rs.r_in && xbf) {
-    const uint16_t *xg = static_cast<const uint16_t *>(p.x);
+    const uint16_t *xg = p.x_import ? p.x_import : static_cast<const uint16_t *>(p.x);
     for (int i = tid; i < H / 8; i += kUT)
-      *reinterpret_cast<uint4 *>(xs_s + 8 * i) = *reinterpret_cast<const uint4 *>(xg + 8 * i);
+      *reinterpret_cast<uint4 *>(xs_s + 8 * i) = __ldcg(reinterpret_cast<const uint4 *>(xg + 8 * i));
     for (int i = H / 8 * 8 + tid; i < H; i += kUT) xs_s[i] = xg[i];
     __syncthreads();
     xsrc = xs_s;
@@ -705,6 +730,7 @@ __global__ void __launch_bounds__(kUT, 1) decode_unit_kernel(const UParams p) {
       if (router && p.wr_smem) mbar_wait_ns(&wr_bar, 0, kUWaitNs);
       if (status & 2) atomicOr(L.err, kErrTimeout);
     }
+    if (!p.x_import) red_relaxed_add64(&L.useq[kUSeqX], 1ull);  // (before the exit: read by later calls only)
     red_release_add64(&L.useq[kUSeqExit], 1ull);
   }
 }
@@ -792,7 +818,7 @@ cudaError_t unit_decode_prepare(Layer &L) {
   return cudaSuccess;
 }
 
-int unit_decode_seq_words() { return kUSeqSlot0 + kUMaxK; }
+int unit_decode_seq_words() { return kUSeqX + 1; }
 
 bool unit_decode_supported(const Layer &L) {
   return L.unit_resident && L.hr && L.hsh && L.useq && L.ulog && unit_shape_ok(L);
@@ -800,13 +826,17 @@ bool unit_decode_supported(const Layer &L) {
 
 cudaError_t launch_decode_unit(const Layer &L, const void *x, moe_dtype xdt, const float *wr, const float *bias,
                                const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
-                               void *out, moe_dtype odt, cudaStream_t stream, const ResidStep *rs) {
+                               void *out, moe_dtype odt, cudaStream_t stream, const ResidStep *rs,
+                               void *x_import) {
   if (!unit_decode_supported(L)) return cudaErrorInvalidConfiguration;
   if (rs && (L.H > kUMaxH || L.H % 8)) return cudaErrorInvalidConfiguration;
+  if (x_import && (rs || xdt != MOE_DT_BF16 || L.H % 8 || !aligned(x_import, 16) || !aligned(x, 16)))
+    return cudaErrorInvalidValue;
   UParams p;
   p.L = L;
   p.x = x;
   p.x_bf16 = xdt == MOE_DT_BF16;
+  p.x_import = static_cast<uint16_t *>(x_import);
   p.rs = rs ? *rs : ResidStep{nullptr, nullptr, 0, nullptr, nullptr, 0.f};
   p.wr = wr;
   p.bias = bias;

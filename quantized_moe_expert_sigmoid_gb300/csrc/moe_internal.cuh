@@ -257,11 +257,16 @@ struct ResidStep {
 };
 cudaError_t launch_decode_unit(const Layer &L, const void *x, moe_dtype xdt, const float *wr, const float *bias,
                                const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
-                               void *out, moe_dtype odt, cudaStream_t stream, const ResidStep *rs = nullptr);
+                               void *out, moe_dtype odt, cudaStream_t stream, const ResidStep *rs = nullptr,
+                               void *x_import = nullptr);
+// x_import (one token, bf16 x in host memory): a device buffer of H bf16
+// values that the one-token kernel copies x into, each CTA its share, before
+// every CTA reads x from it
 cudaError_t launch_decode_fused(const Layer &L, const void *x, moe_dtype xdt, int T,
                                 const float *wr, const float *bias, int64_t bstride,
                                 const int32_t *ids_in, const float *w_in, int32_t *ids_out,
-                                float *w_out, void *out, moe_dtype odt, cudaStream_t stream);
+                                float *w_out, void *out, moe_dtype odt, cudaStream_t stream,
+                                void *x_import = nullptr);
 
 // prefill_tc.cu: 2D tensor-map encoding (driver entry point resolved once).
 cudaError_t encode_2d(CUtensorMap *map, CUtensorMapDataType dt, void *base, uint64_t inner,

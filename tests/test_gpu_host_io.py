@@ -57,3 +57,41 @@ def test_host_call_needs_the_flag():
         moe_layer_forward_routed_host(L.handle, xh, wr, ids, w, out_h)
     assert e.value.name == "MOE_ERR_INVALID_ARG"
     L.close()
+
+
+def test_one_token_host_and_device_calls_interleaved():
+    """At one token the host-buffer call brings x to the device inside the
+    kernel, each CTA its share, behind an arrival counter whose target
+    follows the layer's call count; calls without that step (device x, a
+    4-token batch on another kernel) in any order between them must keep
+    the count right: every host call gives the device call's bits."""
+    wl = synth.WORKLOADS["decode1"]
+    ew = parity.weights(0, 0, wl.E, wl.H, wl.F, 1)
+    c = cases.make_case(wl, T=4, ew=ew, seed=31)
+    L = MoeLayer.from_weights(ew, k=wl.k, scale=wl.scale, max_tokens=16, flags=MOE_FLAG_HOST_IO)
+    x4 = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16)
+    wr = torch.from_numpy(c.wr).cuda()
+    ids = torch.empty((4, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((4, wl.k), dtype=torch.float32, device="cuda")
+    refs = []
+    for t in range(4):
+        o = torch.empty((1, wl.H), dtype=torch.float32, device="cuda")
+        moe_layer_forward_routed(L.handle, x4[t:t + 1].cuda(), wr, ids[:1], w[:1], o)
+        refs.append(o.cpu())
+    out4 = torch.empty((4, wl.H), dtype=torch.float32, device="cuda")
+    xh = [x4[t:t + 1].clone().pin_memory() for t in range(4)]
+    oh = torch.empty((1, wl.H), dtype=torch.float32).pin_memory()
+    for step, t in enumerate([0, 1, 1, 2, 3, 0, 2]):
+        if step % 3 == 1:
+            moe_layer_forward_routed(L.handle, x4.cuda(), wr, ids, w, out4)
+        if step % 2 == 0:
+            o = torch.empty((1, wl.H), dtype=torch.float32, device="cuda")
+            moe_layer_forward_routed(L.handle, xh[t].cuda(), wr, ids[:1], w[:1], o)
+            assert torch.equal(o.cpu(), refs[t])
+        oh.zero_()
+        moe_layer_forward_routed_host(L.handle, xh[t], wr, ids[:1], w[:1], oh)
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(oh, refs[t]), f"step {step}, token {t}"
+    L.check()
+    parity.assert_close_fp32(refs[0].numpy(), parity.oracle_forward(c.x64[:1], c.ids[:1], c.w[:1], ew), "token 0")
+    L.close()
