@@ -77,7 +77,7 @@ METRIC = "MoE-layer tokens/s (expert-weight HBM GB/s as fraction of GB300 peak)"
 # from the ncu captures summarised in profiles/ (None when the kernel changed
 # after its capture).
 NCU_TRAFFIC = {
-    "decode1": 32_125_952,        # decode_unit_kernel<14,2>, ncu dram read + write per launch
+    "decode1": 32_084_480,        # decode_unit_kernel<14,2>, ncu dram read + write per launch
     "decode8": 166_976_256,       # decode_batch_kernel<14,2>, ncu dram read + write per launch
     "prefill4096": 457_219_328,   # grouped_gemm_tc<up/gate>, ncu dram read + write per launch
 }
