@@ -246,12 +246,14 @@ moe_status moe_layer_forward_routed(moe_layer_t layer, const void *x, moe_dtype 
  * on `stream`.  When the device can address a host buffer directly
  * (page-locked or registered memory, 16-byte aligned; on GB300 over the
  * NVLink-C2C link to the Grace host) and the call runs on a single-launch
- * decode kernel (up to 16 tokens), the kernel writes out through it, and at
- * one token the one-token kernel also takes x from there (bf16 x: each CTA
+ * decode kernel (up to 16 tokens), the kernel writes out through it, and
+ * the one-token and batch kernels also take bf16 x from there (each CTA
  * copies its share into the layer's device buffer, so x crosses the link
- * once), so no copy is enqueued.  Otherwise x (for larger batches always: their kernels read all
- * of x in every CTA) and out go through the layer's device buffers with
- * cudaMemcpyAsync (page-locked buffers keep those copies asynchronous).
+ * once; fp32 x is read by every CTA at one token), so no copy is enqueued.
+ * An x or out that is not taken that way (fp32 x above one token, other
+ * kernels, memory the device cannot address) goes through the layer's
+ * device buffers with cudaMemcpyAsync (page-locked buffers keep those
+ * copies asynchronous).
  * Either way x_host and out_host must stay valid and
  * untouched until the stream has passed the call.  router_w,
  * logit_bias, ids and weights are device pointers as for

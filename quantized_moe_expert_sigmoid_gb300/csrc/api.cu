@@ -408,8 +408,8 @@ moe_status moe_dense_forward(moe_layer_t layer, const void *x, moe_dtype x_dtype
   return r;
 }
 
-// moe_layer_forward_routed; x_import as for launch_decode_fused (the
-// host-buffer call passes it at one token, nullptr otherwise)
+// moe_layer_forward_routed; x_import as for launch_decode_fused and
+// launch_decode_batch (the host-buffer call passes it, nullptr otherwise)
 static moe_status forward_routed_impl(moe_layer_t layer, const void *x, moe_dtype x_dtype, int32_t T,
                                       const float *router_w, const float *logit_bias, int64_t bias_row_stride,
                                       int32_t *ids, float *weights, void *out, moe_dtype out_dtype, void *stream,
@@ -435,7 +435,7 @@ static moe_status forward_routed_impl(moe_layer_t layer, const void *x, moe_dtyp
     }
     if (moe::batch_decode_supported(*L, T))
       MOE_CUDA(moe::launch_decode_batch(*L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, nullptr, nullptr,
-                                        ids, weights, out, out_dtype, st),
+                                        ids, weights, out, out_dtype, st, x_import),
                "batch decode");
     else
       MOE_CUDA(moe::launch_decode_fused(*L, x, x_dtype, T, router_w, logit_bias, bias_row_stride, nullptr,
@@ -489,21 +489,23 @@ moe_status moe_layer_forward_routed_host(moe_layer_t layer, const void *x_host, 
   // element once, so they write out through the host buffer itself when the
   // device can address it (page-locked memory; on GB300 over the NVLink-C2C
   // link to the Grace host): no copy-engine round trip after the kernel.
-  // One token on the one-token kernel also takes x from there, so a step is
+  // The one-token and batch kernels also take x from there, so a step is
   // one launch: bf16 x crosses the link once, each CTA bringing its share
   // into the layer's device buffer (every CTA needs all of x; 152 reads of
-  // it over the link cost 5 us more per call); fp32 x is read by every CTA.
-  // Larger batches copy x in once: T x 7 KB per CTA is too much for the link.
+  // it over the link cost 5 us more per call at one token).  fp32 x is read
+  // by every CTA at one token and copied in above it, as is x for the
+  // multi-token kernel of other shapes.
   void *od = nullptr;
   if (moe::batch_decode_supported(*L, T) || moe::fused_decode_supported(*L, T)) {
     od = device_view(out_host);
     if (od && !moe::aligned(od, 16)) od = nullptr;
   }
-  if (od && T == 1 && moe::unit_decode_supported(*L)) {
+  const bool bf16 = x_dtype == MOE_DT_BF16;
+  if (od && ((T == 1 && moe::unit_decode_supported(*L)) || (bf16 && moe::batch_decode_supported(*L, T)))) {
     void *xd = device_view(x_host);
     if (xd && moe::aligned(xd, 16))
       return forward_routed_impl(layer, xd, x_dtype, T, router_w, logit_bias, bias_row_stride, ids, weights, od,
-                                 out_dtype, stream, x_dtype == MOE_DT_BF16 ? L->x_stage : nullptr);
+                                 out_dtype, stream, bf16 ? L->x_stage : nullptr);
   }
   MOE_CUDA(cudaMemcpyAsync(L->x_stage, x_host, n * (x_dtype == MOE_DT_BF16 ? 2 : 4), cudaMemcpyHostToDevice, st),
            "copy x to the device");

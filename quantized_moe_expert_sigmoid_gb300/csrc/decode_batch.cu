@@ -61,14 +61,18 @@ constexpr int kBPre = 4;                      // stages issued before the grid-d
 constexpr int kBMinSlots = 4;                 // ring stages at least (the early ones at most kBPre)
 constexpr uint64_t kBWaitNs = 500000000ull;   // every wait gives up after 0.5 s
 
-// bseq words: [0] exits (G per call); [1 + parity * kBMaxPlan + entry] the
-// entry's unit arrivals in calls of that parity (NB per call)
-constexpr int kBSeqWords = 1 + 2 * kBMaxPlan;
+// bseq words: [0] exits (G per call); [1 + parity * kBSet + entry] the
+// entry's unit arrivals in calls of that parity (NB per call), and
+// [1 + parity * kBSet + kBMaxPlan] the CTAs that have imported their share
+// of x (G per call, host-buffer calls only)
+constexpr int kBSet = kBMaxPlan + 1;
+constexpr int kBSeqWords = 1 + 2 * kBSet;
 
 struct BParams {
   Layer L;
   const void *x;
   int x_bf16;
+  uint16_t *x_import;  // non-null: bf16 x is host memory, brought into this device buffer first
   int T;
   const float *wr, *bias;
   int64_t bstride;
@@ -351,7 +355,9 @@ __device__ __forceinline__ void ug_compute_n(int m, const UgRegs<NST> &w, const 
 
 // NSB: superblocks per up/gate row (H padded = 256 NSB), even.  NL: router
 // logits per lane in the top-k (E <= 32 NL).
-template <int NSB, int NL>
+// XIMP: bf16 x is host memory and is imported first (a separate instance,
+// so that the device-memory kernel carries none of it)
+template <int NSB, int NL, bool XIMP>
 __global__ void __launch_bounds__(kBT, 1)
     decode_batch_kernel(const BParams p, const __grid_constant__ CUtensorMap gu_map) {
   static_assert(NSB % 2 == 0, "two halves of whole superblocks");
@@ -455,20 +461,46 @@ __global__ void __launch_bounds__(kBT, 1)
   const unsigned long long epoch = epoch_s;
   const uint32_t tag = (uint32_t)(epoch + 1);
   const int par = (int)(epoch & 1ull);
-  unsigned long long *ctr = L.bseq + 1 + par * kBMaxPlan;  // this call's arrival counters
+  unsigned long long *ctr = L.bseq + 1 + par * kBSet;  // this call's arrival counters
   if (c == 0)  // the next call's counters (nothing of this call touches them)
-    for (int i = tid; i < kBMaxPlan; i += kBT) L.bseq[1 + (1 - par) * kBMaxPlan + i] = 0ull;
+    for (int i = tid; i < kBSet; i += kBT) L.bseq[1 + (1 - par) * kBSet + i] = 0ull;
+  // x in host memory (the host-buffer call): every CTA copies its share of
+  // x's 16-byte chunks into a device buffer, which the bulk copy below reads
+  // once all G CTAs have (this call's import counter), so x crosses the host
+  // link once per call instead of once per CTA
+  const uint16_t *xg = XIMP ? p.x_import : static_cast<const uint16_t *>(p.x);
+  if constexpr (XIMP) {
+    const unsigned nch = (unsigned)(T * H) / 8u;
+    const int q0 = (int)((unsigned)c * nch / (unsigned)G), q1 = (int)((unsigned)(c + 1) * nch / (unsigned)G);
+    for (int i = tid; i < q1 - q0; i += kBT)
+      reinterpret_cast<uint4 *>(p.x_import)[q0 + i] = reinterpret_cast<const uint4 *>(p.x)[q0 + i];
+    __syncthreads();
+  }
   // bf16 x goes into shared memory in one bulk copy (rows of xw elements),
   // where the router reads it and the quantiser then replaces it in place
   const bool x_smem = p.x_bf16 != 0;
   if (x_smem && tid == 0) {
+    if constexpr (XIMP) {
+      b_red_release_add64(&ctr[kBMaxPlan], 1ull);
+      const uint64_t t0 = global_ns();
+      bool have = false;
+      for (uint32_t poll = 0; !have; ++poll) {
+        have = b_ld_acquire64(&ctr[kBMaxPlan]) >= (unsigned long long)G;
+        if (!have && (poll & 15) == 15 && global_ns() - t0 > kBWaitNs) break;
+      }
+      if (!have) {
+        atomicOr(&status, 1);
+        atomicOr(L.err, kErrTimeout);
+      }
+      // the other CTAs' stores (generic proxy) before the bulk copy's reads
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
     const uint32_t rowb = (uint32_t)H * 2;
     mbar_arrive_expect_tx(&x_bar, rowb * (uint32_t)T);
     if (xw == H)
-      bulk_g2s(xq, p.x, rowb * (uint32_t)T, &x_bar);
+      bulk_g2s(xq, xg, rowb * (uint32_t)T, &x_bar);
     else
-      for (int t = 0; t < T; ++t)
-        bulk_g2s(xq + (size_t)t * xw, reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * H, rowb, &x_bar);
+      for (int t = 0; t < T; ++t) bulk_g2s(xq + (size_t)t * xw, xg + (size_t)t * H, rowb, &x_bar);
   }
 
   // ---- router logits of expert my_e for every token: 32 / T warps per
@@ -1029,11 +1061,16 @@ template <int NSB, int NL>
 cudaError_t batch_prepare_one(Layer &L) {
   cudaFuncAttributes fa;
   int optin = 0;
-  cudaError_t e = cudaFuncGetAttributes(&fa, decode_batch_kernel<NSB, NL>);
+  cudaFuncAttributes fi;
+  cudaError_t e = cudaFuncGetAttributes(&fa, decode_batch_kernel<NSB, NL, false>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fi, decode_batch_kernel<NSB, NL, true>);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, L.device);
   if (e != cudaSuccess) return e;
-  const int limit = optin > (int)fa.sharedSizeBytes ? optin - (int)fa.sharedSizeBytes : 0;
-  e = cudaFuncSetAttribute(decode_batch_kernel<NSB, NL>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+  const int fixed = (int)std::max(fa.sharedSizeBytes, fi.sharedSizeBytes);
+  const int limit = optin > fixed ? optin - fixed : 0;
+  e = cudaFuncSetAttribute(decode_batch_kernel<NSB, NL, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_batch_kernel<NSB, NL, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
   if (e != cudaSuccess) return e;
   L.batch_smem_limit = limit;
   int ns, xw;
@@ -1042,10 +1079,12 @@ cudaError_t batch_prepare_one(Layer &L) {
     L.batch_smem_limit = 0;
     return cudaSuccess;
   }
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_batch_kernel<NSB, NL>, kBT, smem);
+  int per_sm = 0, per_sm_i = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_batch_kernel<NSB, NL, false>, kBT, smem);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_i, decode_batch_kernel<NSB, NL, true>, kBT, smem);
   if (e != cudaSuccess) return e;
-  if (per_sm < 1) L.batch_smem_limit = 0;
+  if (std::min(per_sm, per_sm_i) < 1) L.batch_smem_limit = 0;
   return cudaSuccess;
 }
 
@@ -1066,7 +1105,8 @@ cudaError_t batch_launch(const BParams &p, const CUtensorMap &map, size_t smem, 
   attr[1].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.L.coop ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, decode_batch_kernel<NSB, NL>, p, map);
+  return p.x_import ? cudaLaunchKernelEx(&cfg, decode_batch_kernel<NSB, NL, true>, p, map)
+                    : cudaLaunchKernelEx(&cfg, decode_batch_kernel<NSB, NL, false>, p, map);
 }
 
 }  // namespace
@@ -1105,14 +1145,18 @@ bool batch_decode_supported(const Layer &L, int T) {
 
 cudaError_t launch_decode_batch(const Layer &L, const void *x, moe_dtype xdt, int T, const float *wr,
                                 const float *bias, int64_t bstride, const int32_t *ids_in, const float *w_in,
-                                int32_t *ids_out, float *w_out, void *out, moe_dtype odt, cudaStream_t stream) {
+                                int32_t *ids_out, float *w_out, void *out, moe_dtype odt, cudaStream_t stream,
+                                void *x_import) {
   if (!batch_decode_supported(L, T)) return cudaErrorInvalidConfiguration;
+  if (x_import && (xdt != MOE_DT_BF16 || L.H % 8 || !aligned(x_import, 16) || !aligned(x, 16)))
+    return cudaErrorInvalidValue;
   BParams p;
   size_t smem;
   if (!batch_plan(L, T, p.ns, p.xw, smem)) return cudaErrorInvalidConfiguration;
   p.L = L;
   p.x = x;
   p.x_bf16 = xdt == MOE_DT_BF16;
+  p.x_import = static_cast<uint16_t *>(x_import);
   p.T = T;
   p.wr = wr;
   p.bias = bias;

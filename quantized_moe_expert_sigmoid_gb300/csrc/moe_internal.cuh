@@ -241,7 +241,8 @@ int64_t batch_decode_log_words(const Layer &L);
 bool batch_decode_supported(const Layer &L, int T);
 cudaError_t launch_decode_batch(const Layer &L, const void *x, moe_dtype xdt, int T, const float *wr,
                                 const float *bias, int64_t bstride, const int32_t *ids_in, const float *w_in,
-                                int32_t *ids_out, float *w_out, void *out, moe_dtype odt, cudaStream_t stream);
+                                int32_t *ids_out, float *w_out, void *out, moe_dtype odt, cudaStream_t stream,
+                                void *x_import = nullptr);
 int unit_decode_seq_words();
 bool unit_decode_supported(const Layer &L);
 // The layer input of one trunk step, formed inside the one-token kernel:

@@ -1,9 +1,8 @@
 """moe_layer_forward_routed_host: x and out in pinned host memory, the copies
 enqueued with the layer call.  Its output must equal the device-memory call's
 bit for bit (the same kernels run on the same values), for the one-token
-kernel (x and out through the host mapping), the batch kernel (x copied in,
-out through the host mapping) and the multi-launch path (both copied), bf16
-and fp32 out."""
+and batch kernels (x imported inside the kernel, out through the host
+mapping) and the multi-launch path (both copied), bf16 and fp32 out."""
 import numpy as np
 import pytest
 
@@ -94,4 +93,41 @@ def test_one_token_host_and_device_calls_interleaved():
         assert torch.equal(oh, refs[t]), f"step {step}, token {t}"
     L.check()
     parity.assert_close_fp32(refs[0].numpy(), parity.oracle_forward(c.x64[:1], c.ids[:1], c.w[:1], ew), "token 0")
+    L.close()
+
+
+def test_batch_host_calls_with_changing_x():
+    """The batch kernel takes bf16 x from host memory the same way (each CTA
+    copies its share into the layer's device buffer, one arrival counter,
+    then one bulk copy of x into shared memory).  x changes on every call,
+    with one-token host calls and device calls between, so a stale or
+    partly written import would show: every host call gives the device
+    call's bits for its own x."""
+    wl = synth.WORKLOADS["decode1"]
+    ew = parity.weights(0, 0, wl.E, wl.H, wl.F, 1)
+    c = cases.make_case(wl, T=12, ew=ew, seed=33)
+    L = MoeLayer.from_weights(ew, k=wl.k, scale=wl.scale, max_tokens=16, flags=MOE_FLAG_HOST_IO)
+    x = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16)
+    wr = torch.from_numpy(c.wr).cuda()
+    batches = [(0, 4), (4, 8), (0, 12), (3, 5), (5, 6)]  # the last one is a single token
+    ids = torch.empty((12, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((12, wl.k), dtype=torch.float32, device="cuda")
+    refs = []
+    for a, b in batches:
+        o = torch.empty((b - a, wl.H), dtype=torch.bfloat16, device="cuda")
+        moe_layer_forward_routed(L.handle, x[a:b].cuda(), wr, ids[:b - a], w[:b - a], o)
+        refs.append(o.cpu())
+    xh = [x[a:b].clone().pin_memory() for a, b in batches]
+    for step, i in enumerate([0, 1, 2, 0, 4, 1, 3, 2, 4, 3, 0]):
+        a, b = batches[i]
+        if step % 4 == 3:
+            o = torch.empty((b - a, wl.H), dtype=torch.bfloat16, device="cuda")
+            moe_layer_forward_routed(L.handle, xh[i].cuda(), wr, ids[:b - a], w[:b - a], o)
+        oh = torch.zeros((b - a, wl.H), dtype=torch.bfloat16).pin_memory()
+        moe_layer_forward_routed_host(L.handle, xh[i], wr, ids[:b - a], w[:b - a], oh)
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(oh, refs[i]), f"step {step}, tokens {a}..{b}"
+    L.check()
+    ref = parity.oracle_forward(c.x64, c.ids, c.w, ew)
+    parity.assert_close_bf16(refs[2].float().numpy(), ref, "12 tokens")
     L.close()
