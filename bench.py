@@ -23,8 +23,11 @@ layer calls, and the timed region replays it until exactly --steps steps
 have run.  The spread of the step time (p10 / median / p90) comes from a
 further >= 10 replays of the same graph, each timed on its own.  `e2e` times
 the same calls eagerly, one moe_layer_forward_routed_host call per step: the
-input copied from pinned host memory, the layer, and the output copied back,
-enqueued by the library.
+input taken from pinned host memory, the layer, and the output written back
+to pinned host memory, all inside the timed region.  Up to 16 tokens the
+decode kernels bring x across the host link themselves and store out through
+it; above that the library enqueues copies.  The byte counts are those of x
+and out either way.
 
 --impl reference times the CPU oracle (fp64, single thread) on the same
 workload and metric.
