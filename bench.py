@@ -81,7 +81,7 @@ METRIC = "MoE-layer tokens/s (expert-weight HBM GB/s as fraction of GB300 peak)"
 # after its capture).
 NCU_TRAFFIC = {
     "decode1": 32_084_480,        # decode_unit_kernel<14,2>, ncu dram read + write per launch
-    "decode8": 166_976_256,       # decode_batch_kernel<14,2>, ncu dram read + write per launch
+    "decode8": None,              # decode_batch_kernel<14,2,false>: changed after its capture (counter layout)
     "prefill4096": 457_219_328,   # grouped_gemm_tc<up/gate>, ncu dram read + write per launch
 }
 
